@@ -1,0 +1,238 @@
+/*
+ * epd_oracle.c -- plain, slow, single-threaded CPU oracle for the single-GPU
+ * MoE expert-parallel token permute / unpermute path.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline / reference arm may load this library. The product path never
+ * links, imports or calls it, and it shares no code, header or table with the
+ * CUDA library: every function below is written out from the definitions on the
+ * pages, in plain loops, with no blocking, fusion or reordering.
+ *
+ * Sources (page title, section):
+ *   [P1] "参考sglang代码，重构vllm021中EP高吞吐代码，消除空泡问题"
+ *        (refactoring vLLM's EP high-throughput path after SGLang), sections
+ *        2.2 / 2.2.4 (pre_permute + ep_scatter: "scan, then scatter") and
+ *        3.3 (deepgemm_moe_permute: m_indices / inv_perm initialised to -1).
+ *   [P2] "高性能专家并行（EP）内核解剖学解读" (anatomy of high-performance EP
+ *        kernels), sections "任务设定与数据流" (8 GPUs on 2 nodes, 2 experts per
+ *        GPU, top-2 of 16) and "5. 缓冲区布局与发送" (buffer layout by prefix sum).
+ *   [P3] "[MoE] Deepseek的All-to-all通信: DeepEP代码解读" (reading DeepEP),
+ *        section "Dispatch" (get_dispatch_layout and dispatch docstrings;
+ *        "combine is similar to dispatch").
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - expert e belongs to simulated rank e / (E/R); rank r to simulated RDMA
+ *     node r / (R/N) (contiguous blocks);
+ *   - per-rank and per-node counts count tokens, once per rank / node;
+ *   - slots inside one expert are assigned in token-major (t, then j) order;
+ *   - output_index is -1 for a pair with no selection; m_indices is -1 on the
+ *     rows [P, capacity) that no pair fills;
+ *   - the combine is the weighted sum over the valid pairs of a token, formed
+ *     here in fp64 and rounded once to bf16 (round to nearest, ties to even);
+ *     a token with no valid pair gives +0.
+ *
+ * Build: gcc -O2 -ffp-contract=off -std=c11 -fPIC -shared (single-threaded).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+enum {
+    ORC_OK = 0,
+    ORC_ERR_INVALID_ARG = 1,
+    ORC_ERR_INVALID_EXPERT = 4,
+    ORC_ERR_CAPACITY = 6,
+};
+
+/* Simulated topology: [P2] "任务设定与数据流" places 2 experts on each of 8 GPUs
+ * and the 8 GPUs on 2 nodes; contiguous blocks are the plain reading. */
+static int rank_of_expert(int64_t e, int E, int R) { return (int)(e / (E / R)); }
+static int node_of_rank(int r, int R, int N) { return r / (R / N); }
+
+static int check_topology(int T, int k, int E, int R, int N) {
+    if (T < 0 || k < 0 || E < 1 || R < 1 || N < 1) return ORC_ERR_INVALID_ARG;
+    if (E % R != 0 || R % N != 0) return ORC_ERR_INVALID_ARG;
+    return ORC_OK;
+}
+
+/*
+ * Dispatch layout -- [P3] "Dispatch", get_dispatch_layout docstring:
+ *   num_tokens_per_expert[e] = number of (t, j) with topk_idx[t, j] == e;
+ *   is_token_in_rank[t, r]   = token t is sent to rank r;
+ *   num_tokens_per_rank[r]   = number of tokens sent to rank r;
+ *   num_tokens_per_rdma_rank[n] = number of tokens sent to RDMA node n.
+ * -1 means "no selection". Any other id outside [0, E) is rejected.
+ * tokens_per_rdma_rank and is_token_in_rank may be NULL (not computed).
+ */
+int oracle_dispatch_layout(const int64_t *topk_idx, int T, int k, int E, int R, int N,
+                           int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                           int32_t *tokens_per_rdma_rank, uint8_t *is_token_in_rank) {
+    int rc = check_topology(T, k, E, R, N);
+    if (rc != ORC_OK) return rc;
+    for (int64_t i = 0; i < (int64_t)T * k; ++i) {
+        int64_t e = topk_idx[i];
+        if (e < -1 || e >= E) return ORC_ERR_INVALID_EXPERT;
+    }
+
+    for (int e = 0; e < E; ++e) tokens_per_expert[e] = 0;
+    for (int r = 0; r < R; ++r) tokens_per_rank[r] = 0;
+    if (tokens_per_rdma_rank)
+        for (int n = 0; n < N; ++n) tokens_per_rdma_rank[n] = 0;
+
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t e = topk_idx[(int64_t)t * k + j];
+            if (e >= 0) tokens_per_expert[e] += 1;
+        }
+        /* token t is sent to rank r if any of its selections lives on r */
+        for (int r = 0; r < R; ++r) {
+            int in_rank = 0;
+            for (int j = 0; j < k; ++j) {
+                int64_t e = topk_idx[(int64_t)t * k + j];
+                if (e >= 0 && rank_of_expert(e, E, R) == r) in_rank = 1;
+            }
+            if (is_token_in_rank) is_token_in_rank[(int64_t)t * R + r] = (uint8_t)in_rank;
+            tokens_per_rank[r] += in_rank;
+        }
+        /* token t is sent to node n if it is sent to any rank of n */
+        if (tokens_per_rdma_rank) {
+            for (int n = 0; n < N; ++n) {
+                int in_node = 0;
+                for (int j = 0; j < k; ++j) {
+                    int64_t e = topk_idx[(int64_t)t * k + j];
+                    if (e >= 0 && node_of_rank(rank_of_expert(e, E, R), R, N) == n) in_node = 1;
+                }
+                tokens_per_rdma_rank[n] += in_node;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Expert offsets -- [P2] "5. 缓冲区布局与发送": the first source starts at index
+ * 0 and each next one starts where the previous one ended, i.e. the exclusive
+ * prefix sum of the counts. [P1] 2.2.4: ep_scatter "scans, then scatters"
+ * into expert_start_loc. *total = sum of all counts.
+ */
+int oracle_scan_offsets(const int32_t *tokens_per_expert, int E, int32_t *expert_start_loc,
+                        int32_t *total) {
+    if (E < 1) return ORC_ERR_INVALID_ARG;
+    int64_t run = 0;
+    for (int e = 0; e < E; ++e) {
+        expert_start_loc[e] = (int32_t)run;
+        run += tokens_per_expert[e];
+    }
+    *total = (int32_t)run;
+    return ORC_OK;
+}
+
+/*
+ * Permute (ep_scatter) -- [P1] 2.2 and 3.3: each token row (and its fp8 scale
+ * row) is copied, byte for byte, to one row of the expert-contiguous buffer per
+ * selected expert; m_indices[row] = expert of that row, output_index[t, j] =
+ * the row that pair (t, j) went to. Pairs are visited token-major, so rows
+ * within one expert follow (t, j) order. Pairs with no selection get
+ * output_index = -1; rows [P, capacity) get m_indices = -1 ([P1] 3.3: the
+ * buffer is pre-filled with -1 so unwritten rows are skipped downstream).
+ *
+ * x: T rows of row_bytes bytes; x_scale: T rows of scale_cols floats, or NULL.
+ * out: capacity rows of row_bytes; out_scale: capacity rows of scale_cols.
+ * Rows of out / out_scale at and beyond P are left untouched.
+ */
+int oracle_permute(const uint8_t *x, int64_t row_bytes, const float *x_scale, int scale_cols,
+                   const int64_t *topk_idx, int T, int k, int E,
+                   const int32_t *expert_start_loc, int64_t capacity,
+                   uint8_t *out, float *out_scale, int32_t *m_indices, int32_t *output_index) {
+    if (T < 0 || k < 0 || E < 1 || row_bytes < 0 || capacity < 0) return ORC_ERR_INVALID_ARG;
+    int32_t fill_count[E];
+    for (int e = 0; e < E; ++e) fill_count[e] = 0;
+    int64_t filled = 0;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t e = topk_idx[(int64_t)t * k + j];
+            if (e < -1 || e >= E) return ORC_ERR_INVALID_EXPERT;
+            if (e == -1) {
+                output_index[(int64_t)t * k + j] = -1;
+                continue;
+            }
+            int64_t s = (int64_t)expert_start_loc[e] + fill_count[e];
+            fill_count[e] += 1;
+            if (s < 0 || s >= capacity) return ORC_ERR_CAPACITY;
+            output_index[(int64_t)t * k + j] = (int32_t)s;
+            m_indices[s] = (int32_t)e;
+            memcpy(out + s * row_bytes, x + (int64_t)t * row_bytes, (size_t)row_bytes);
+            if (x_scale != NULL && scale_cols > 0)
+                memcpy(out_scale + s * scale_cols, x_scale + (int64_t)t * scale_cols,
+                       (size_t)scale_cols * sizeof(float));
+            filled += 1;
+        }
+    }
+    for (int64_t s = filled; s < capacity; ++s) m_indices[s] = -1;
+    return ORC_OK;
+}
+
+/*
+ * bf16 from a double, round to nearest, ties to even, written from the format's
+ * definition (8 significant bits, fp32's exponent range, subnormal spacing
+ * 2^-133): scale to the spacing of the value's binade, round the scaled value to
+ * an integer with ties to even, scale back. Overflow gives infinity.
+ */
+uint16_t oracle_bf16_from_double(double v) {
+    if (isnan(v)) return (uint16_t)0x7FC0;
+    uint16_t sign = signbit(v) ? (uint16_t)0x8000 : (uint16_t)0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    int ex;
+    (void)frexp(a, &ex);          /* a in [2^(ex-1), 2^ex) */
+    int lead = ex - 1;
+    if (lead < -126) lead = -126; /* below the normal range the spacing stays 2^-133 */
+    double spacing = ldexp(1.0, lead - 7);
+    double scaled = a / spacing;  /* exact: division by a power of two */
+    double rounded = nearbyint(scaled); /* default mode: nearest, ties to even */
+    double result = rounded * spacing;
+    if (result >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    float f = (float)result;      /* exact: result has <= 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)((bits >> 16) & 0x7FFF));
+}
+
+double oracle_double_from_bf16(uint16_t b) {
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Unpermute (combine) -- [P3] "Dispatch": the weights travel with the tokens
+ * (topk_weights, fp32) and combine is the reverse of dispatch. For every token
+ * t and column h:
+ *     y[t, h] = bf16( sum over j with output_index[t, j] != -1 of
+ *                     topk_weights[t, j] * expert_out[output_index[t, j], h] )
+ * The sum is formed in fp64 in j order and rounded once. A token with no valid
+ * pair gives +0.
+ */
+int oracle_unpermute(const uint16_t *expert_out, int64_t capacity, const int32_t *output_index,
+                     const float *topk_weights, int T, int k, int H, uint16_t *y) {
+    if (T < 0 || k < 0 || H < 0 || capacity < 0) return ORC_ERR_INVALID_ARG;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int32_t s = output_index[(int64_t)t * k + j];
+            if (s < -1 || (int64_t)s >= capacity) return ORC_ERR_CAPACITY;
+        }
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t s = output_index[(int64_t)t * k + j];
+                if (s < 0) continue;
+                acc += (double)topk_weights[(int64_t)t * k + j] *
+                       oracle_double_from_bf16(expert_out[(int64_t)s * H + h]);
+            }
+            y[(int64_t)t * H + h] = oracle_bf16_from_double(acc);
+        }
+    }
+    return ORC_OK;
+}

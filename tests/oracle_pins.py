@@ -1,0 +1,286 @@
+"""Checks that pin the CPU oracle to what the pages and the mathematics fix.
+
+Each ``check_*`` function takes the oracle module as an argument so that the
+same checks can be run against deliberately broken copies of the oracle (see
+``test_oracle_mutants.py``). None of them re-types the oracle's formulas: the
+expected values come from the hand-worked example in ``tests/golden``, from an
+independent definition (a sort of the (expert, token, slot) pairs), from
+invariants, from closed forms of the combine, or from torch's own bf16
+rounding.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+from collections import Counter
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_golden(name="hand_example.json"):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def token_id_rows(T, row_bytes=16):
+    """Rows whose bytes spell the token index, so a permuted row names its source."""
+    rows = np.zeros((T, row_bytes), np.uint8)
+    for t in range(T):
+        rows[t, :4] = np.frombuffer(np.int32(t).tobytes(), np.uint8)
+        rows[t, 4:] = (t * 7 + np.arange(row_bytes - 4)) % 251
+    return rows
+
+
+def rows_to_token_ids(rows):
+    return [int(np.frombuffer(r[:4].tobytes(), np.int32)[0]) for r in rows]
+
+
+# ----------------------------------------------------------------------------- hand example
+def check_hand_example(orc):
+    g = load_golden()
+    topk = np.array(g["topk_idx"], np.int64)
+    E, R, N, k = g["E"], g["R"], g["N"], g["k"]
+    T = topk.shape[0]
+    lay = orc.dispatch_layout(topk, E, R, N)
+    assert lay["tokens_per_expert"].tolist() == g["tokens_per_expert"]
+    assert lay["tokens_per_rank"].tolist() == g["tokens_per_rank"]
+    assert lay["tokens_per_rdma_rank"].tolist() == g["tokens_per_rdma_rank"]
+    sets = [sorted(np.nonzero(row)[0].tolist()) for row in lay["is_token_in_rank"]]
+    assert sets == g["is_token_in_rank_sets"]
+    start, total = orc.scan_offsets(lay["tokens_per_expert"])
+    assert start.tolist() == g["expert_start_loc"]
+    assert total == g["total_rows"]
+    x = token_id_rows(T)
+    per = orc.permute(x, None, topk, E, start, T * k)
+    assert per["output_index"].tolist() == g["output_index"]
+    assert per["m_indices"].tolist() == g["m_indices"]
+    assert rows_to_token_ids(per["out"][:total]) == g["permuted_source_tokens"]
+
+
+# ----------------------------------------------------------------------------- independent definition
+def reference_by_sort(topk, E, R, N):
+    """Layout and slots from an independent formulation: sort all valid pairs by
+    (expert, token, slot) -- the buffer is then read off in order."""
+    T, k = topk.shape
+    pairs = [(int(topk[t, j]), t, j) for t in range(T) for j in range(k) if topk[t, j] >= 0]
+    order = sorted(pairs)
+    slot = {(t, j): s for s, (e, t, j) in enumerate(order)}
+    output_index = [[slot.get((t, j), -1) for j in range(k)] for t in range(T)]
+    m_indices = [e for (e, _, _) in order] + [-1] * (T * k - len(order))
+    cnt = Counter(e for (e, _, _) in order)
+    counts = [cnt.get(e, 0) for e in range(E)]
+    epr = E // R
+    rpn = R // N
+    token_ranks = [{int(e) // epr for e in topk[t] if e >= 0} for t in range(T)]
+    token_nodes = [{r // rpn for r in rs} for rs in token_ranks]
+    per_rank = [sum(r in rs for rs in token_ranks) for r in range(R)]
+    per_node = [sum(n in ns for ns in token_nodes) for n in range(N)]
+    first = {}
+    for s, (e, _, _) in enumerate(order):
+        first.setdefault(e, s)
+    # start of an expert = number of pairs of lower experts
+    start = [sum(counts[:e]) for e in range(E)]
+    return dict(output_index=output_index, m_indices=m_indices, counts=counts, start=start,
+                per_rank=per_rank, per_node=per_node, token_ranks=token_ranks, total=len(order))
+
+
+def check_against_sort(orc, topk, E, R, N):
+    T, k = topk.shape
+    ref = reference_by_sort(topk, E, R, N)
+    lay = orc.dispatch_layout(topk, E, R, N)
+    assert lay["tokens_per_expert"].tolist() == ref["counts"], "counts"
+    assert lay["tokens_per_rank"].tolist() == ref["per_rank"], "per_rank"
+    assert lay["tokens_per_rdma_rank"].tolist() == ref["per_node"], "per_node"
+    sets = [set(np.nonzero(row)[0].tolist()) for row in lay["is_token_in_rank"]]
+    assert sets == ref["token_ranks"], "is_token_in_rank"
+    start, total = orc.scan_offsets(lay["tokens_per_expert"])
+    assert start.tolist() == ref["start"], "start"
+    assert total == ref["total"], "total"
+    x = token_id_rows(T)
+    per = orc.permute(x, None, topk, E, start, T * k)
+    assert per["output_index"].tolist() == ref["output_index"], "output_index"
+    assert per["m_indices"].tolist() == ref["m_indices"], "m_indices"
+    src = rows_to_token_ids(per["out"][:total])
+    for s, (e, t, j) in enumerate(sorted((int(topk[t, j]), t, j) for t in range(T)
+                                         for j in range(k) if topk[t, j] >= 0)):
+        assert src[s] == t, "permuted row source"
+
+
+def check_bruteforce(orc, T, k, E, R, N, limit=None):
+    """Every topk_idx in {-1..E-1}^(T x k) (with repeats) against the sort definition."""
+    n = 0
+    for flat in itertools.product(range(-1, E), repeat=T * k):
+        check_against_sort(orc, np.array(flat, np.int64).reshape(T, k), E, R, N)
+        n += 1
+        if limit is not None and n >= limit:
+            break
+    return n
+
+
+# ----------------------------------------------------------------------------- invariants
+def check_invariants(orc, topk, E, R, N, row_bytes=32, with_scale=True, capacity=None):
+    T, k = topk.shape
+    if capacity is None:
+        capacity = T * k
+    valid = topk >= 0
+    P = int(valid.sum())
+    lay = orc.dispatch_layout(topk, E, R, N)
+    cnt = lay["tokens_per_expert"].astype(np.int64)
+    assert cnt.sum() == P                                    # counts sum to the valid picks
+    start, total = orc.scan_offsets(lay["tokens_per_expert"])
+    assert total == P
+    if E > 0:
+        assert start[0] == 0
+        assert np.all(np.diff(start.astype(np.int64)) == cnt[:-1])   # offsets tile [0, P)
+        assert int(start[-1]) + int(cnt[-1]) == P
+    rng = np.random.default_rng(T * 131 + k)
+    x = rng.integers(0, 256, size=(T, row_bytes), dtype=np.uint8)
+    sc = rng.standard_normal((T, 3)).astype(np.float32) if with_scale else None
+    per = orc.permute(x, sc, topk, E, start, capacity)
+    oi = per["output_index"]
+    mi = per["m_indices"]
+    assert np.all(oi[~valid] == -1)
+    slots = oi[valid]
+    assert sorted(slots.tolist()) == list(range(P))         # bijection onto [0, P)
+    assert np.all(mi[slots] == topk[valid])                  # row -> expert
+    assert np.all(mi[P:] == -1)
+    assert np.array_equal(per["out"][slots], np.repeat(x, k, axis=0)[valid.reshape(-1)])
+    if with_scale:
+        assert np.array_equal(per["out_scale"][slots], np.repeat(sc, k, axis=0)[valid.reshape(-1)])
+    # slots grow with (t, j) inside each expert
+    for e in np.unique(topk[valid]):
+        s_e = oi[topk == e]            # row-major order of (t, j)
+        assert np.all(np.diff(s_e) > 0)
+        assert s_e[0] == start[e]
+    per_rank = lay["tokens_per_rank"].astype(np.int64)
+    in_rank = lay["is_token_in_rank"]
+    assert np.array_equal(in_rank.sum(axis=0), per_rank)
+    epr, rpn = E // R, R // N
+    per_node = lay["tokens_per_rdma_rank"].astype(np.int64)
+    for r in range(R):
+        assert per_rank[r] <= cnt[r * epr:(r + 1) * epr].sum()
+    for n in range(N):
+        block = per_rank[n * rpn:(n + 1) * rpn]
+        assert block.sum() >= per_node[n] >= (block.max() if block.size else 0)
+        assert per_node[n] <= T
+    return lay, start, per
+
+
+# ----------------------------------------------------------------------------- combine
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_combine_identity(orc, T=40, H=64, k=4, E=8, p_invalid=0.3, seed=5):
+    """Identity experts and weights summing to 1: y equals x bit for bit, and a
+    token whose picks were all dropped gives +0."""
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(T, E, generator=g)
+    topk = torch.argsort(-logits, dim=1, stable=True)[:, :k]
+    valid = torch.rand(T, k, generator=g) >= p_invalid
+    valid[0] = False                                  # one token with no pick at all
+    topk = torch.where(valid, topk, torch.full_like(topk, -1)).numpy().astype(np.int64)
+    picked = torch.gather(logits, 1, torch.as_tensor(np.maximum(topk, 0)))
+    w = torch.softmax(picked.masked_fill(~valid, float("-inf")), dim=1)
+    w = torch.nan_to_num(w, nan=0.0).float().numpy()
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    xb = bf16_bits(x)
+    res = orc.run_path(xb.view(np.uint8), None, topk, w, E, 1, 1)
+    y = res["y"]
+    has = valid.numpy().any(axis=1)
+    assert np.array_equal(y[has], xb[has])
+    assert np.all(y[~has] == 0)
+
+
+def check_combine_one_hot(orc, T=24, H=32, k=3, E=6, seed=9):
+    """One weight 1, the others 0: y is the selected expert-output row exactly."""
+    rng = np.random.default_rng(seed)
+    topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int64)
+    hot = rng.integers(0, k, size=T)
+    w = np.zeros((T, k), np.float32)
+    w[np.arange(T), hot] = 1.0
+    x = np.zeros((T, 2 * H), np.uint8)
+    lay = orc.dispatch_layout(topk, E, 1, 1)
+    start, _ = orc.scan_offsets(lay["tokens_per_expert"])
+    per = orc.permute(x, None, topk, E, start, T * k)
+    eo = bf16_bits(torch.randn(T * k, H, generator=torch.Generator().manual_seed(seed))
+                   .to(torch.bfloat16))
+    y = orc.unpermute(eo, per["output_index"], w)
+    sel = per["output_index"][np.arange(T), hot]
+    assert np.array_equal(y, eo[sel])
+
+
+def _bf16_of_fraction(q: Fraction) -> int:
+    """Round an exact rational to bf16 with torch's float32 -> bf16 conversion.
+    Only used where q is exactly representable in float32, so the one rounding
+    is torch's."""
+    f = np.float32(float(q))
+    assert Fraction(float(f)) == q
+    return int(bf16_bits(torch.tensor([f]).to(torch.bfloat16))[0])
+
+
+def _bf16_bits_of(v: float) -> int:
+    return int(bf16_bits(torch.tensor([v], dtype=torch.float32).to(torch.bfloat16))[0])
+
+
+def check_combine_exact_sums(orc):
+    """Dyadic weights and values: the exact weighted sum is known as a fraction;
+    it includes bf16 round-to-nearest-even ties in both directions, cancellation
+    to zero, and a sign change."""
+    one = 1.0
+    cases = [
+        # (values (bf16-exact), weights) -> exact sum
+        ([1.0, 2.0 ** -8], [1.0, 1.0]),                 # 1 + 2^-8: tie -> even (1.0)
+        ([1.0, 3 * 2.0 ** -8], [1.0, 1.0]),             # 1 + 3*2^-8: tie -> even (1 + 2^-6)
+        ([1.0, 2.0 ** -8], [1.0, 1.5]),                 # above the tie -> up
+        ([3.0, -1.5], [0.5, 1.0]),                      # 1.5 - 1.5 = 0
+        ([2.0, -3.0], [0.25, 0.5]),                     # 0.5 - 1.5 = -1
+        ([0.75, 0.125, -0.0625], [0.5, 0.25, 2.0]),     # 0.375 + 0.03125 - 0.125
+        ([one] * 8, [0.125] * 8),                       # eight eighths
+        ([float(2 ** 120), float(2 ** 120)], [1.0, 1.0]),   # large magnitude
+    ]
+    for vals, ws in cases:
+        k = len(vals)
+        eo = np.array([[_bf16_bits_of(v)] for v in vals], np.uint16)      # [k, 1]
+        oi = np.arange(k, dtype=np.int32).reshape(1, k)
+        w = np.array([ws], np.float32)
+        y = orc.unpermute(eo, oi, w)
+        exact = sum(Fraction(wv) * Fraction(v) for wv, v in zip(ws, vals))
+        assert int(y[0, 0]) == _bf16_of_fraction(exact), (vals, ws)
+    # the order and sign of terms matter: w * x with x negative
+    eo = np.array([[_bf16_bits_of(-2.5)], [_bf16_bits_of(1.25)]], np.uint16)
+    y = orc.unpermute(eo, np.array([[1, 0]], np.int32), np.array([[2.0, 0.5]], np.float32))
+    assert int(y[0, 0]) == _bf16_bits_of(2.0 * 1.25 + 0.5 * -2.5)
+
+
+def check_bf16_rounding(orc, n=20000, seed=3):
+    """The oracle's bf16 rounding against torch's float32 -> bf16 conversion."""
+    rng = np.random.default_rng(seed)
+    mant = rng.integers(0, 1 << 23, size=n, dtype=np.int64)
+    expo = rng.integers(0, 255, size=n, dtype=np.int64)        # incl. subnormals, no inf/nan
+    sign = rng.integers(0, 2, size=n, dtype=np.int64)
+    bits = ((sign << 31) | (expo << 23) | mant).astype(np.uint32)
+    # force exact ties and near-ties on a quarter of them
+    tie = (bits & ~np.uint32(0xFFFF)) | np.uint32(0x8000)
+    bits[: n // 4] = tie[: n // 4]
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    want = bf16_bits(torch.from_numpy(f.copy()).to(torch.bfloat16))
+    got = np.array([orc.bf16_from_double(float(v)) for v in f], np.uint16)
+    assert np.array_equal(got, want)
+    # every finite bf16 pattern survives a round trip through double
+    for b in range(0, 1 << 16, 97):
+        if (b & 0x7F80) == 0x7F80:
+            continue
+        assert orc.bf16_from_double(orc.double_from_bf16(b)) == b
+
+
+def check_combine_all(orc):
+    check_combine_identity(orc)
+    check_combine_one_hot(orc)
+    check_combine_exact_sums(orc)
