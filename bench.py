@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Benchmark of the single-GPU MoE expert-parallel permute / unpermute path.
+
+One step = one pass of the whole path over one batch: ep_dispatch_layout ->
+ep_scan_offsets -> ep_permute -> ep_unpermute, all on one stream with no host
+synchronisation in between. The metric is source tokens per second, with the
+achieved HBM bandwidth (algorithmic bytes / time) against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl epd|reference]
+                    [--workload dsv3_fp8|prefill_bf16|skew_bf16|tiny|decode_fp8]
+
+--impl reference times the CPU oracle (plain single-threaded C) on a bounded
+token sample of the same workload. With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU; the time is the maximum over ranks.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "permute+unpermute tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    on = device if (device is not None and dist.get_backend() == "nccl") else torch.device("cpu")
+    t = torch.tensor([float(value)], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units every rank processed divided by the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
+# ----------------------------------------------------------------------------- bytes of the path
+def algorithmic_bytes(case, P: int, M: int) -> dict:
+    """Minimum HBM bytes of each step: every row read once and written once per
+    pick, plus the index, weight and count traffic."""
+    T, H, k, E, R = case.T, case.H, case.k, case.E, case.R
+    fp8 = case.dtype == "fp8"
+    b = 1 if fp8 else 2
+    sc = (H // 128) * 4 if fp8 else 0
+    layout = T * k * 8 + T * R + 3 * E * 4
+    scan = 2 * E * 4 + 4
+    permute = T * H * b + T * sc + P * H * b + P * sc + T * k * 8 + T * k * 4 + M * 4
+    unpermute = P * H * 2 + T * H * 2 + T * k * 4 + T * k * 4
+    return dict(ep_dispatch_layout=layout, ep_scan_offsets=scan, ep_permute=permute,
+                ep_unpermute=unpermute)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(name: str) -> str:
+    p = os.path.join(ROOT, "unpermute_ep_dispatch_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, source: str, workload: str, units: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled to `units`
+    tokens, or None when the kernel changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[kernel]
+    except Exception:
+        return None
+    if e.get("source_sha256_16") != kernel_source_hash(source) or e.get("workload") != workload:
+        return None
+    return float(e["dram_bytes_per_launch"]) * units / float(e["tokens"])
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML (read only)
+    in a background thread while the timed region runs."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if not self._handle(cuda_index):
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _handle(self, cuda_index):
+        import torch
+        try:
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            u = ("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid
+            if self.nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.h)) == 0:
+                return True
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = cuda_index
+        if vis:
+            try:
+                idx = int(vis.split(",")[cuda_index])
+            except ValueError:
+                idx = cuda_index
+        return self.nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) == 0
+
+    def _run(self):
+        mhz = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        mw = ctypes.c_uint()
+        get_reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                r = reasons.value if get_reasons(self.h, ctypes.byref(reasons)) == 0 else 0
+                p = mw.value / 1000.0 if self.nv.nvmlDeviceGetPowerUsage(
+                    self.h, ctypes.byref(mw)) == 0 else None
+                self.samples.append((int(mhz.value), int(r), p))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "source": "nvml" if self.ok else "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[1]
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle")
+        powers = [s[2] for s in self.samples if s[2] is not None]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz),
+                "power_w_max": max(powers) if powers else None, "source": "nvml"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def time_oracle(name: str, tokens: int, min_seconds: float, max_reps: int = 1000, seed=None):
+    """The CPU oracle on a `tokens`-token instance of the workload, repeated until
+    min_seconds of work; returns (tokens per second, reps, seconds per rep)."""
+    import oracle
+    from unpermute_ep_dispatch_gb300 import workloads
+    case = workloads.make_case(name, T=tokens, seed=seed)
+    args = _oracle_args(case)
+    oracle.build()
+    oracle.run_path(*args[0], **args[1])          # warm (page in, build)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run_path(*args[0], **args[1])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return tokens * reps / el, reps, el / reps
+
+
+def _oracle_args(case):
+    import numpy as np
+    import torch
+
+    def u8rows(t):
+        t = t.contiguous()
+        return t.view(torch.uint8).numpy().reshape(t.shape[0], -1)
+    eo = None
+    if case.expert_out is not None:
+        eo = case.expert_out.contiguous().view(torch.int16).numpy().view(np.uint16)
+    xs = None if case.x_scale is None else case.x_scale.numpy()
+    return ((u8rows(case.x), xs, case.topk_idx.numpy(), case.topk_weights.numpy(), case.E,
+             case.R, case.N), dict(expert_out=eo))
+
+
+# ----------------------------------------------------------------------------- the GPU arm
+def run_epd(args, rank, world, local):
+    import torch
+    import unpermute_ep_dispatch_gb300 as epd
+    from unpermute_ep_dispatch_gb300 import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    init_dist(world, "nccl")
+    epd.load_library()
+    name = args.workload
+    case = workloads.make_case(name, T=args.tokens)
+    T, H, k, E, R, N = case.T, case.H, case.k, case.E, case.R, case.N
+    M = case.capacity
+    stream = torch.cuda.Stream(dev)
+
+    # device-resident inputs and outputs (allocated once; the step allocates nothing)
+    topk = case.topk_idx.to(dev)
+    w = case.topk_weights.to(dev)
+    x = case.x.to(dev)
+    xs = None if case.x_scale is None else case.x_scale.to(dev)
+    eo = None if case.expert_out is None else case.expert_out.to(dev)
+    ws = epd.new_workspace(T, k, E, R, N, dev)
+    status = epd.new_status(dev)
+    per_e = torch.empty(E, dtype=torch.int32, device=dev)
+    per_r = torch.empty(R, dtype=torch.int32, device=dev)
+    per_n = torch.empty(N, dtype=torch.int32, device=dev)
+    itr = torch.empty(T, R, dtype=torch.bool, device=dev)
+    start = torch.empty(E, dtype=torch.int32, device=dev)
+    total = torch.empty(1, dtype=torch.int32, device=dev)
+    out = torch.empty(M, H, dtype=x.dtype, device=dev)
+    out_scale = None if xs is None else torch.empty(M, H // 128, dtype=torch.float32, device=dev)
+    m_idx = torch.empty(M, dtype=torch.int32, device=dev)
+    out_idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        epd.ep_dispatch_layout(topk, E, R, N, ws, status, tokens_per_expert=per_e,
+                               tokens_per_rank=per_r, tokens_per_rdma_rank=per_n,
+                               is_token_in_rank=itr, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        epd.ep_scan_offsets(per_e, status, expert_start_loc=start, total_rows=total,
+                            stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        epd.ep_permute(x, xs, topk, E, start, ws, status, capacity_rows=M, out=out,
+                       out_scale=out_scale, m_indices=m_idx, output_index=out_idx, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        epd.ep_unpermute(out if eo is None else eo, out_idx, w, status, y=y, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    epd.check_status(status, "warm-up")
+    P = int(total.item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks.stop()
+    epd.check_status(status, "timed steps")
+    ms_local = t_start.elapsed_time(t_end)
+    ms = reduce_max(ms_local, world, dev)
+    names = ["ep_dispatch_layout", "ep_scan_offsets", "ep_permute", "ep_unpermute"]
+    per_kernel_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                     for j, n in enumerate(names)}
+
+    # ---- end to end through the public API: host inputs in, host result out, every step
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: None if t is None else t.contiguous().pin_memory()  # noqa: E731
+        h_topk, h_w, h_x, h_xs, h_eo = (pin(case.topk_idx), pin(case.topk_weights),
+                                        pin(case.x), pin(case.x_scale), pin(case.expert_out))
+        h_y = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_topk, h_w, h_x, h_xs, h_eo)
+                  if t is not None)
+        d2h = h_y.numel() * h_y.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                topk.copy_(h_topk, non_blocking=True)
+                w.copy_(h_w, non_blocking=True)
+                x.copy_(h_x, non_blocking=True)
+                if xs is not None:
+                    xs.copy_(h_xs, non_blocking=True)
+                if eo is not None:
+                    eo.copy_(h_eo, non_blocking=True)
+                step()
+                h_y.copy_(y, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(args.steps, 50))
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = reduce_max(a.elapsed_time(b), world, dev) / e2e_steps
+        e2e = {"value": whole_job_rate(T, world, e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": e2e_ms}
+        epd.check_status(status, "e2e steps")
+
+    # ---- roofline of the dominant kernel and of the whole path
+    bytes_k = algorithmic_bytes(case, P, M)
+    peak, peak_src = load_peaks()
+    dom = max(names, key=lambda n: bytes_k[n])
+    dom_src = {"ep_unpermute": "unpermute.cu", "ep_permute": "permute.cu",
+               "ep_dispatch_layout": "layout.cu", "ep_scan_offsets": "scan.cu"}[dom]
+    achieved = bytes_k[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
+    ms_per_step = ms / args.steps
+    path_bytes = sum(bytes_k.values())
+    path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
+    kernels = {n: {"us": round(per_kernel_ms[n] * 1e3, 2), "bytes": bytes_k[n],
+                   "gbs": round(bytes_k[n] / (per_kernel_ms[n] * 1e-3) / 1e9, 1),
+                   "frac": round(bytes_k[n] / (per_kernel_ms[n] * 1e-3) / 1e9 / peak, 4)}
+               for n in names}
+
+    result = {
+        "metric": METRIC,
+        "value": whole_job_rate(T * args.steps, world, ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded routing, rows and expert outputs; no dataset)",
+        "config": {"workload": name, "tokens": T, "hidden": H, "top_k": k, "experts": E,
+                   "simulated_ranks": R, "simulated_rdma_nodes": N,
+                   "rows": "fp8_e4m3 + f32 scale per 128 columns" if case.dtype == "fp8"
+                   else "bf16",
+                   "expert_out": "bf16 identity (permuted rows)" if eo is None else "bf16 seeded",
+                   "capacity_rows": M, "valid_pairs": P,
+                   "l2": f"no flush: {path_bytes / 1e6:.0f} MB moved per step > 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "hbm": {"path_gbs": round(path_gbs, 1), "path_bytes": path_bytes,
+                "frac": round(path_gbs / peak, 4), "peak_gbs": peak, "peak_source": peak_src},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(dom, dom_src, name, T),
+                     "algorithmic_bytes": bytes_k[dom], "peak_source": peak_src},
+        "kernels": kernels,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, reps, sec = time_oracle(name, args.cpu_tokens, args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{name} routing at T={args.cpu_tokens} tokens (same H, k, E, R, N), "
+                      f"{reps} full-path reps in {reps * sec:.1f} s, single-threaded C"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- the reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: rank 0 only; other ranks exit at once."""
+    if rank != 0:
+        return
+    import oracle
+    from unpermute_ep_dispatch_gb300 import workloads
+    name = args.workload
+    cfg = workloads.CONFIGS[name]
+    T_s = args.cpu_tokens
+    case = workloads.make_case(name, T=T_s)
+    a, kw = _oracle_args(case)
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle.run_path(*a, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_path(*a, **kw)
+    el = time.perf_counter() - t0
+    v = T_s * args.steps / el
+    result = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded routing, rows and expert outputs; no dataset)",
+        "config": {"workload": name, "tokens": args.tokens or cfg["T"], "hidden": cfg["H"],
+                   "top_k": cfg["k"], "experts": cfg["E"], "simulated_ranks": cfg["R"],
+                   "simulated_rdma_nodes": cfg["N"], "parallelism": "CPU, 1 thread"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{name} routing at T={T_s} tokens per step (same H, k, E, "
+                                   f"R, N), single-threaded C oracle"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["epd", "reference"], default="epd")
+    ap.add_argument("--workload", default="dsv3_fp8")
+    ap.add_argument("--tokens", type=int, default=None, help="override T (smaller instances)")
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "epd":
+        print("note: at least 3 warm-up steps are used", file=sys.stderr)
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_epd(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * epd.h -- C ABI of libepd: single-GPU MoE expert-parallel token permute and
+ * unpermute for GB300 (sm_103a).
+ *
+ * The path, in the order a caller runs it on one stream:
+ *   1. ep_dispatch_layout  counts per expert / simulated rank / simulated RDMA
+ *                          node and the is_token_in_rank mask;
+ *   2. ep_scan_offsets     expert_start_loc = exclusive prefix sum of the counts;
+ *   3. ep_permute          ep_scatter: token rows into the expert-contiguous
+ *                          buffer, with m_indices and output_index;
+ *   4. ep_unpermute        combine: the topk-weighted sum of each token's expert
+ *                          output rows, accumulated in fp32.
+ * Nothing in between goes back to the host: every count, offset and total stays
+ * in device memory, and the permuted buffer is sized at the T*k upper bound.
+ *
+ * Conventions shared by every call:
+ *   - The caller owns all memory. libepd never allocates or frees device or
+ *     host memory. Every pointer argument except the stream is a device
+ *     pointer unless stated otherwise.
+ *   - Every call is asynchronous on the caller's stream, does not synchronise
+ *     and touches no host memory (the stream replaces DeepEP's previous_event /
+ *     async_finish pair).
+ *   - The return value reports argument errors, found on the host before any
+ *     launch (EPD_ERR_INVALID_ARG, EPD_ERR_UNSUPPORTED), and launch errors
+ *     (EPD_ERR_CUDA). A call that returns an error has launched nothing.
+ *   - Errors that depend on the data (an expert id outside [-1, E), a slot
+ *     outside the buffer, a look-back wait that gave up) are written to the
+ *     caller's device word `status` with an atomic compare-and-swap from 0, so
+ *     the first error sticks until the caller clears the word. Kernels never
+ *     trap: the offending pair is skipped and the call completes.
+ *   - Sizes: T = num_tokens >= 0, k = num_topk in [0, EPD_MAX_TOPK],
+ *     E = num_experts in [1, EPD_MAX_EXPERTS], R = num_ranks with E % R == 0,
+ *     N = num_rdma_ranks with R % N == 0, T*k <= INT32_MAX.
+ *     Expert e lives on simulated rank e / (E/R); rank r on node r / (R/N).
+ *
+ * Page references (page title, section):
+ *   [P1] "参考sglang代码，重构vllm021中EP高吞吐代码，消除空泡问题"
+ *   [P2] "高性能专家并行（EP）内核解剖学解读"
+ *   [P3] "[MoE] Deepseek的All-to-all通信: DeepEP代码解读"
+ */
+#ifndef EPD_H
+#define EPD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define EPD_API __attribute__((visibility("default")))
+#else
+#define EPD_API
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *epd_stream_t;
+
+typedef enum {
+    EPD_OK = 0,
+    EPD_ERR_INVALID_ARG = 1,    /* bad size, null or misaligned pointer, mismatched workspace */
+    EPD_ERR_UNSUPPORTED = 2,    /* valid but beyond a documented limit */
+    EPD_ERR_CUDA = 3,           /* a launch failed; cudaGetLastError() has the cause */
+    EPD_ERR_INVALID_EXPERT = 4, /* (status word) topk_idx held an id outside [-1, E) */
+    EPD_ERR_TIMEOUT = 5,        /* (status word) a bounded look-back wait gave up */
+    EPD_ERR_CAPACITY = 6,       /* (status word) a slot fell outside [0, capacity_rows) */
+} epd_status_t;
+
+typedef enum {
+    EPD_BF16 = 0,      /* rows of H bfloat16 values (2H bytes), H % 8 == 0 */
+    EPD_FP8_E4M3 = 1,  /* rows of H float8_e4m3fn values (H bytes) plus H/128 fp32
+                          scales per row, H % 128 == 0 */
+} epd_dtype_t;
+
+#define EPD_MAX_EXPERTS 4096
+#define EPD_MAX_TOPK 64
+
+/* Human-readable name of a status code (static string; never NULL). */
+EPD_API const char *epd_status_string(int code);
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+EPD_API int epd_version(void);
+
+/*
+ * Workspace size in bytes for one layout -> permute chain over T tokens, k
+ * picks, E experts, R ranks and N nodes. The workspace holds the per-pair rank
+ * inside its expert (T*k int32) and the per-tile state of the layout's
+ * single-pass look-back. Returns 0 for invalid sizes. Host-only arithmetic.
+ */
+EPD_API size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
+                           int num_rdma_ranks);
+
+/*
+ * Zero-fills `workspace` (device, `bytes` long) on `stream`. A workspace must
+ * be zero-filled once before its first use; the layout call keeps it reusable
+ * from then on (its look-back state is tagged with a call counter). A
+ * workspace serves one stream at a time: two calls that overlap on the GPU
+ * and share a workspace race.
+ */
+EPD_API epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_stream_t stream);
+
+/*
+ * Step 1 -- dispatch layout. [P3] "Dispatch", get_dispatch_layout docstring:
+ * from topk_idx [T, k] int64 (row-major; -1 = no selection) compute
+ *   tokens_per_expert    [E] int32: number of (t, j) with topk_idx[t, j] == e;
+ *   tokens_per_rank      [R] int32: number of tokens with a pick on rank r
+ *                                   (a token counts once per rank);
+ *   tokens_per_rdma_rank [N] int32: number of tokens with a pick on node n
+ *                                   (once per node); may be NULL (DeepEP
+ *                                   returns None for one node);
+ *   is_token_in_rank  [T, R] uint8: 1 if token t has a pick on rank r, else 0
+ *                                   (torch.bool layout); may be NULL.
+ * and, in `workspace` (epd_workspace_bytes(T, k, E, R, N) bytes), the rank of
+ * every pair among the pairs of its expert in token-major (t, then j) order,
+ * which ep_permute turns into slots. The ranks come from one single-pass
+ * decoupled look-back scan over token tiles, so the result does not depend on
+ * the order in which blocks run. Ids outside [-1, E) set
+ * EPD_ERR_INVALID_EXPERT in *status and are treated as -1.
+ */
+EPD_API epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                int num_experts, int num_ranks, int num_rdma_ranks,
+                                int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                                int32_t *tokens_per_rdma_rank, uint8_t *is_token_in_rank,
+                                void *workspace, int32_t *status, epd_stream_t stream);
+
+/*
+ * Step 2 -- expert offsets. [P2] "5. 缓冲区布局与发送" (the first source starts
+ * at 0, each next one where the previous ended) and [P1] 2.2.4 (ep_scatter
+ * scans, then scatters): expert_start_loc[e] = sum of tokens_per_expert[e'] for
+ * e' < e; *total_rows (device int32) = the sum of all counts. A negative count
+ * sets EPD_ERR_INVALID_ARG in *status.
+ */
+EPD_API epd_status_t ep_scan_offsets(const int32_t *tokens_per_expert, int num_experts,
+                             int32_t *expert_start_loc, int32_t *total_rows, int32_t *status,
+                             epd_stream_t stream);
+
+/*
+ * Step 3 -- permute (ep_scatter). [P1] 2.2 (ep_scatter into input_tensor,
+ * input_tensor_scale, m_indices, output_index) and 3.3 (m_indices pre-set to
+ * -1 so that unwritten rows are skipped): for every pair (t, j) with expert
+ * e = topk_idx[t, j] != -1, its slot is s = expert_start_loc[e] + (rank of the
+ * pair inside e, from ep_dispatch_layout's workspace) and
+ *   out[s, :]         = x[t, :]        (row bytes copied verbatim),
+ *   out_scale[s, :]   = x_scale[t, :]  (fp8 only, H/128 floats),
+ *   m_indices[s]      = e,
+ *   output_index[t,j] = s;
+ * pairs with no selection get output_index = -1, and m_indices[s] = -1 for
+ * every s in [P, capacity_rows), P = number of valid pairs. Rows of out and
+ * out_scale at and beyond P are not written.
+ *   x:            [T, H] dtype rows, 16-byte aligned;
+ *   x_scale:      [T, H/128] float32 for EPD_FP8_E4M3, NULL for EPD_BF16;
+ *   out:          [capacity_rows, H] dtype, 16-byte aligned;
+ *   out_scale:    [capacity_rows, H/128] float32 (fp8) or NULL (bf16);
+ *   m_indices:    [capacity_rows] int32;  output_index: [T, k] int32;
+ *   capacity_rows >= T*k (the exact-allocation upper bound with alignment 1),
+ *   capacity_rows <= INT32_MAX.
+ * `workspace` must hold the layout of the same topk_idx (same T and k); a
+ * mismatch sets EPD_ERR_INVALID_ARG in *status and writes nothing.
+ */
+EPD_API epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float *x_scale,
+                        const int64_t *topk_idx, int num_tokens, int num_topk, int hidden,
+                        int num_experts, const int32_t *expert_start_loc, const void *workspace,
+                        int64_t capacity_rows, void *out, float *out_scale, int32_t *m_indices,
+                        int32_t *output_index, int32_t *status, epd_stream_t stream);
+
+/*
+ * Step 4 -- unpermute (combine). [P3] "Dispatch" (combine is the reverse of
+ * dispatch; topk_weights are fp32 [T, k]):
+ *   y[t, h] = bf16( sum over j with output_index[t, j] != -1, in j order, of
+ *                   topk_weights[t, j] * expert_out[output_index[t, j], h] )
+ * with every product and sum in fp32 (no fused multiply-add) and one
+ * round-to-nearest-even to bf16. A token with no valid pair gets +0.
+ *   expert_out:   [capacity_rows, H] bfloat16, 16-byte aligned;
+ *   output_index: [T, k] int32 (from ep_permute); topk_weights: [T, k] float32;
+ *   y:            [T, H] bfloat16, 16-byte aligned; H % 8 == 0.
+ * A slot outside [-1, capacity_rows) sets EPD_ERR_CAPACITY and is skipped.
+ */
+EPD_API epd_status_t ep_unpermute(const void *expert_out, int64_t capacity_rows,
+                          const int32_t *output_index, const float *topk_weights, int num_tokens,
+                          int num_topk, int hidden, void *y, int32_t *status, epd_stream_t stream);
+
+/*
+ * Test hook for failure detection, not part of the path: runs ep_dispatch_layout
+ * with the look-back wait bounded by `spin_limit` polls and with token tile
+ * `stalled_tile` never publishing its state, so that every later tile's wait
+ * runs out. The call still completes; *status then holds EPD_ERR_TIMEOUT and
+ * the counts are meaningless. The workspace stays reusable afterwards.
+ */
+EPD_API epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                          int num_experts, int num_ranks, int num_rdma_ranks,
+                                          int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                                          int32_t *tokens_per_rdma_rank,
+                                          uint8_t *is_token_in_rank, void *workspace,
+                                          int32_t *status, int stalled_tile,
+                                          uint32_t spin_limit, epd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EPD_H */

@@ -1,0 +1,221 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Bit-exact for counts, is_token_in_rank, offsets, m_indices, output_index and the
+permuted rows / scales; the bf16 combine within 1e-3 + 1e-2 |ref| per element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import unpermute_ep_dispatch_gb300 as epd
+from epd_paths import GpuPath, bits16, compare, oracle_path
+from unpermute_ep_dispatch_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from unpermute_ep_dispatch_gb300 import build
+    build.build()
+    epd.load_library()
+
+
+def run_both(case, capacity=None, stream=None):
+    g = GpuPath(case, capacity=capacity, stream=stream)
+    g.step()
+    got = g.results()
+    want = oracle_path(case, capacity=capacity)
+    return got, want, g
+
+
+# ----------------------------------------------------------------------------- the five workloads
+@pytest.mark.parametrize("name", ["tiny", "prefill_bf16", "dsv3_fp8", "skew_bf16"])
+def test_workload_full_size(name):
+    case = workloads.make_case(name)
+    got, want, _ = run_both(case)
+    err = compare(got, want)
+    print(f"{name}: P={want['total_rows']} combine error {err:.3f} of tolerance")
+
+
+def test_decode_steps():
+    for i in range(8):
+        case = workloads.make_case("decode_fp8", seed=1000 + i)
+        got, want, _ = run_both(case)
+        compare(got, want)
+
+
+def test_identity_experts_give_back_x():
+    """Weights that sum to 1 over identity experts: y == x exactly (0 for no pick)."""
+    case = workloads.make_case("prefill_bf16")
+    g = GpuPath(case)
+    g.step()
+    r = g.results()
+    xb = bits16(case.x)
+    has = (case.topk_idx >= 0).any(dim=1).numpy()
+    assert np.array_equal(r["y"][has], xb[has])
+    assert np.all(r["y"][~has] == 0)
+
+
+# ----------------------------------------------------------------------------- edge cases
+EDGE_T = [0, 1, 2, 3, 31, 33, 65, 257, 1000]
+EDGE_TOPO = [(1, 1, 1), (2, 2, 1), (16, 8, 2), (256, 32, 4)]   # (E, R, N)
+
+
+@pytest.mark.parametrize("T", EDGE_T)
+@pytest.mark.parametrize("k", [1, 2, 8])
+@pytest.mark.parametrize("topo", EDGE_TOPO)
+@pytest.mark.parametrize("p_invalid", [0.0, 0.5, 1.0])
+def test_edge_matrix_bf16(T, k, topo, p_invalid):
+    E, R, N = topo
+    case = workloads.make_random_case(T=T, H=136, k=k, E=E, R=R, N=N, dtype="bf16",
+                                      seed=T * 7 + k * 131 + E, routing="repeats",
+                                      p_invalid=p_invalid, experts="random")
+    got, want, _ = run_both(case)
+    compare(got, want)
+
+
+@pytest.mark.parametrize("T", [0, 1, 33, 257])
+@pytest.mark.parametrize("k,E,R,N", [(1, 16, 8, 2), (8, 256, 32, 4), (6, 64, 8, 1)])
+@pytest.mark.parametrize("H", [128, 384])
+def test_edge_fp8(T, k, E, R, N, H):
+    case = workloads.make_random_case(T=T, H=H, k=k, E=E, R=R, N=N, dtype="fp8",
+                                      seed=T + k + H, routing="uniform", p_invalid=0.25,
+                                      experts="random")
+    got, want, _ = run_both(case)
+    compare(got, want)
+
+
+def test_large_topk_and_repeated_experts():
+    """k = 64 (the limit) over 4 experts: long runs of the same expert in a row."""
+    case = workloads.make_random_case(T=300, H=64, k=64, E=4, R=2, N=1, dtype="bf16", seed=4,
+                                      routing="repeats", p_invalid=0.1, experts="random")
+    got, want, _ = run_both(case)
+    compare(got, want)
+
+
+def test_many_experts():
+    case = workloads.make_random_case(T=700, H=64, k=8, E=4096, R=512, N=8, dtype="bf16",
+                                      seed=6, routing="uniform", experts="random")
+    got, want, _ = run_both(case)
+    compare(got, want)
+
+
+def test_capacity_above_tk_fills_tail():
+    case = workloads.make_random_case(T=200, H=64, k=4, E=16, R=4, N=2, dtype="bf16", seed=8,
+                                      routing="uniform", p_invalid=0.3, experts="random")
+    got, want, _ = run_both(case, capacity=200 * 4 + 333)
+    compare(got, want)
+    assert np.all(got["m_indices"][want["total_rows"]:] == -1)
+
+
+def test_ragged_hidden_bf16():
+    for H in (8, 24, 7176):
+        case = workloads.make_random_case(T=45, H=H, k=3, E=8, R=4, N=2, dtype="bf16", seed=H,
+                                          routing="uniform", experts="random")
+        got, want, _ = run_both(case)
+        compare(got, want)
+
+
+def test_side_stream():
+    s = torch.cuda.Stream()
+    case = workloads.make_case("tiny")
+    with torch.cuda.stream(s):
+        got, want, _ = run_both(case, stream=s)
+    compare(got, want)
+
+
+# ----------------------------------------------------------------------------- determinism & reuse
+def test_deterministic_and_workspace_reuse():
+    case = workloads.make_case("dsv3_fp8", T=3000)
+    g = GpuPath(case)
+    g.step()
+    first = g.results()
+    for _ in range(3):
+        g.step()
+    again = g.results()
+    for key in first:
+        a, b = first[key], again[key]
+        if isinstance(a, np.ndarray):
+            P = first["total_rows"]
+            if key in ("out", "out_scale"):
+                a, b = a[:P], b[:P]
+            assert np.array_equal(a, b), key
+        else:
+            assert a == b, key
+
+
+def test_workspace_shared_across_shapes():
+    """One workspace, sized for the largest shape, reused for smaller ones."""
+    big = workloads.make_case("dsv3_fp8", T=2048)
+    ws = epd.new_workspace(2048, 8, 256, 32, 4)
+    for T in (2048, 17, 1500, 1):
+        case = workloads.make_case("dsv3_fp8", T=T, seed=T)
+        g = GpuPath(case)
+        g.ws = ws[: epd.epd_workspace_bytes(T, 8, 256, 32, 4)]
+        g.step()
+        compare(g.results(), oracle_path(case))
+    del big
+
+
+# ----------------------------------------------------------------------------- failure paths
+def test_invalid_expert_ids_are_reported_and_skipped():
+    case = workloads.make_random_case(T=150, H=64, k=4, E=16, R=8, N=2, dtype="bf16", seed=2,
+                                      routing="uniform", experts="random")
+    bad = case.topk_idx.clone()
+    bad[3, 1] = 16
+    bad[77, 0] = -5
+    bad[149, 3] = 1 << 40
+    case_bad = workloads.Case(**{**case.__dict__, "topk_idx": bad})
+    g = GpuPath(case_bad)
+    g.step()
+    got = g.results()
+    assert got["status"] == epd.EPD_ERR_INVALID_EXPERT
+    clean = torch.where((bad >= -1) & (bad < 16), bad, torch.full_like(bad, -1))
+    want = oracle_path(case, topk_override=clean)
+    compare(got, want, check_status=False)
+
+
+def test_lookback_wait_gives_up_and_workspace_recovers():
+    """A tile that never publishes: later tiles stop waiting after a bounded number
+    of polls and report EPD_ERR_TIMEOUT; the next normal call is correct."""
+    case = workloads.make_case("dsv3_fp8", T=2048)
+    g = GpuPath(case)
+    epd._binding.epd_test_layout_stalled_tile(g.topk, case.E, case.R, case.N, g.ws, g.status,
+                                              stalled_tile=0, spin_limit=2000)
+    torch.cuda.synchronize()
+    assert int(g.status.item()) == epd.EPD_ERR_TIMEOUT
+    g.status.zero_()
+    g.step()
+    compare(g.results(), oracle_path(case))
+
+
+def test_permute_rejects_workspace_of_another_layout():
+    a = workloads.make_case("tiny")
+    b = workloads.make_case("tiny", T=32, seed=5)
+    ga = GpuPath(a)
+    ga.layout()
+    gb = GpuPath(b)
+    gb.ws = ga.ws[: gb.ws.numel()]
+    gb.per_e.zero_()
+    gb.scan()
+    gb.output_index.fill_(123)
+    gb.permute()
+    torch.cuda.synchronize()
+    assert int(gb.status.item()) == epd.EPD_ERR_INVALID_ARG
+    assert torch.all(gb.output_index == 123)
+
+
+def test_binding_validates_tensors():
+    case = workloads.make_case("tiny")
+    g = GpuPath(case)
+    with pytest.raises(ValueError):
+        epd.ep_dispatch_layout(g.topk.to(torch.int32), 16, 8, 2, g.ws, g.status)
+    with pytest.raises(ValueError):
+        epd.ep_dispatch_layout(g.topk, 16, 8, 2, g.ws[:16], g.status)
+    with pytest.raises(epd.EpdError):
+        epd.ep_dispatch_layout(g.topk, 16, 3, 1, g.ws, g.status)
+    with pytest.raises(ValueError):
+        epd.ep_unpermute(g.out.float(), g.output_index, g.w, g.status)

@@ -1,0 +1,127 @@
+// epd_common.cuh -- helpers shared by libepd's CUDA translation units:
+// workspace layout, argument checks, PTX wrappers for the memory-model
+// operations the look-back needs, and 16-byte streaming loads / stores.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "epd.h"
+
+namespace epd {
+
+// ---------------------------------------------------------------------------- workspace
+// Byte layout of the caller's workspace. The header and the per-pair ranks sit
+// at fixed offsets that depend on T*k only, so ep_permute (which is not given
+// R and N) finds them; the look-back state follows.
+struct WsHeader {
+    uint32_t ticket;       // next token tile to hand out (dynamic tile order)
+    uint32_t done;         // number of layout blocks that finished this call
+    uint32_t epoch;        // call counter; look-back states carry it
+    int32_t total_pairs;   // P of the last layout call
+    int32_t num_tokens;    // T of the last layout call
+    int32_t num_topk;      // k of the last layout call
+    uint32_t pad[10];
+};
+static_assert(sizeof(WsHeader) == 64, "header is one 64-byte block");
+
+constexpr size_t kAlign = 256;
+constexpr int kLayoutThreads = 256;
+constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kMaxPairsPerTile = 512;
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Tokens per layout tile: at most 512 (token, pick) pairs and at most 256 tokens.
+__host__ __device__ inline int layout_tile_tokens(int k) {
+    int t = k > 0 ? kMaxPairsPerTile / k : 256;
+    if (t < 1) t = 1;
+    if (t > 256) t = 256;
+    return t;
+}
+
+struct WsLayout {
+    size_t header_off, pair_rank_off, state_off, agg_off, incl_off, total;
+    int tiles, cols, cols_pad;
+};
+
+__host__ __device__ inline size_t ws_pair_rank_off() { return kAlign; }
+
+__host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N) {
+    WsLayout w;
+    int tile = layout_tile_tokens(k);
+    w.tiles = T > 0 ? (T + tile - 1) / tile : 1;
+    w.cols = E + R + N;
+    w.cols_pad = (int)align_up((size_t)w.cols, 32);
+    w.header_off = 0;
+    w.pair_rank_off = ws_pair_rank_off();
+    w.state_off = align_up(w.pair_rank_off + (size_t)T * (size_t)k * 4, kAlign);
+    w.agg_off = align_up(w.state_off + (size_t)w.tiles * 4, kAlign);
+    w.incl_off = align_up(w.agg_off + (size_t)w.tiles * w.cols_pad * 4, kAlign);
+    w.total = align_up(w.incl_off + (size_t)w.tiles * w.cols_pad * 4, kAlign);
+    return w;
+}
+
+// ---------------------------------------------------------------------------- host checks
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+
+inline bool topology_ok(int T, int k, int E, int R, int N) {
+    if (T < 0 || k < 0 || k > EPD_MAX_TOPK) return false;
+    if (E < 1 || E > EPD_MAX_EXPERTS) return false;
+    if (R < 1 || R > E || E % R != 0) return false;
+    if (N < 1 || N > R || R % N != 0) return false;
+    if ((int64_t)T * (int64_t)k > INT32_MAX) return false;
+    return true;
+}
+
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+inline epd_status_t launch_status() {
+    return cudaGetLastError() == cudaSuccess ? EPD_OK : EPD_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------- device helpers
+__device__ __forceinline__ void report(int32_t *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Streaming 16-byte load that does not allocate in L1 (each row is read once).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st16(void *p, const uint4 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+}  // namespace epd

@@ -1,0 +1,408 @@
+// layout.cu -- step 1 of the path: the dispatch layout.
+//
+// "[MoE] Deepseek的All-to-all通信: DeepEP代码解读", section "Dispatch"
+// (get_dispatch_layout docstring): from topk_idx [T, k] (-1 = no selection)
+// count the tokens sent to each expert, each rank and each RDMA node, and mark
+// is_token_in_rank. The pages skip the kernel body; this one is designed for
+// sm_103a from the definition.
+//
+// One block per token tile (tile order from an atomic ticket, so a block only
+// ever waits on blocks that are already running). Inside a tile:
+//   * each warp walks a contiguous run of the tile's (token, pick) pairs in
+//     row-major order; lanes holding the same expert find each other with
+//     __match_any_sync, and the lowest of them adds the group's size to the
+//     warp's private shared-memory histogram (warp-aggregated, no atomics);
+//   * an exclusive scan across the warps' histograms gives each pair its rank
+//     among the tile's pairs of the same expert, in (t, j) order;
+//   * the tile's counts (experts, ranks, nodes) are published and the prefix
+//     over earlier tiles is read with a single-pass decoupled look-back: a
+//     warp polls the states of up to 32 earlier tiles at once and stops at the
+//     nearest one that has published its inclusive prefix;
+//   * prefix + warp base + rank inside the warp = the pair's rank inside its
+//     expert over the whole batch, stored in the workspace for ep_permute;
+//   * the tile that holds the last ticket writes the totals.
+// Every value is an integer sum, so the outputs are the same whichever order
+// the blocks run in. Waits are bounded: a wait that runs out sets
+// EPD_ERR_TIMEOUT and the block carries on.
+#include "epd_common.cuh"
+
+namespace epd {
+namespace {
+
+constexpr uint32_t kStateAgg = 1;   // tile published its own counts
+constexpr uint32_t kStateIncl = 2;  // tile published counts of itself and all earlier tiles
+constexpr uint32_t kDefaultSpinLimit = 1u << 19;  // polls with back-off: about a second
+
+struct LayoutArgs {
+    const int64_t *topk;
+    int T, k, E, R, N, epr, rpn;
+    int32_t *per_expert, *per_rank, *per_node;
+    uint8_t *in_rank;
+    WsHeader *hdr;
+    int32_t *pair_rank;
+    uint32_t *state;
+    int32_t *agg, *incl;
+    int tiles, tile_tokens, cols, cols_pad;
+    int32_t *status;
+    int stalled_tile;
+    uint32_t spin_limit;
+};
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
+    extern __shared__ int4 smem_raw[];
+    int *hw = reinterpret_cast<int *>(smem_raw);           // [warps][E] histograms -> warp bases
+    int *col_agg = hw + kLayoutWarps * a.E;                // [cols_pad] this tile's counts
+    int *col_excl = col_agg + a.cols_pad;                  // [cols_pad] counts of earlier tiles
+    int *pair_e = col_excl + a.cols_pad;                   // [tile pairs] expert or -1
+    int *pair_r = pair_e + a.tile_tokens * a.k;            // [tile pairs] rank inside the warp
+    __shared__ int s_tile;
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_win_aggs, s_win_incl, s_win_done;
+    __shared__ int s_red[kLayoutWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_tile = (int)atomicAdd(&a.hdr->ticket, 1u);
+        s_epoch = ld_relaxed_gpu(&a.hdr->epoch);
+    }
+    for (int i = tid; i < kLayoutWarps * a.E; i += kLayoutThreads) hw[i] = 0;
+    for (int i = tid; i < a.cols_pad; i += kLayoutThreads) {
+        col_agg[i] = 0;
+        col_excl[i] = 0;
+    }
+    __syncthreads();
+    const int tile = s_tile;
+    const uint32_t epoch = s_epoch;
+    const uint32_t tag = epoch << 2;
+    const int t0 = tile * a.tile_tokens;
+    const int ntok = max(0, min(a.tile_tokens, a.T - t0));
+    const int npairs = ntok * a.k;
+    const int64_t pair0 = (int64_t)t0 * a.k;
+
+    // (1) warp-aggregated histograms over contiguous runs of 32-pair chunks
+    const int nchunks = (npairs + 31) >> 5;
+    const int cpw = (nchunks + kLayoutWarps - 1) / kLayoutWarps;
+    int *my_hist = hw + warp * a.E;
+    const int c_end = min(nchunks, (warp + 1) * cpw);
+    for (int c = warp * cpw; c < c_end; ++c) {
+        const int p = (c << 5) + lane;
+        int e = -1;
+        if (p < npairs) {
+            const int64_t v = a.topk[pair0 + p];
+            if (v >= 0 && v < a.E) e = (int)v;
+            else if (v != -1) report(a.status, EPD_ERR_INVALID_EXPERT);
+            pair_e[p] = e;
+        }
+        const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
+        if (e >= 0) {
+            const uint32_t peers = __match_any_sync(valid, e);
+            const int before = __popc(peers & lanemask_lt());
+            const int base = my_hist[e];
+            pair_r[p] = base + before;
+            __syncwarp(peers);
+            if (before == 0) my_hist[e] = base + __popc(peers);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // (2) exclusive scan across warps per expert; tile count per expert
+    for (int e = tid; e < a.E; e += kLayoutThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int v = hw[w * a.E + e];
+            hw[w * a.E + e] = run;
+            run += v;
+        }
+        col_agg[e] = run;
+    }
+    // (3) ranks and nodes: a token counts once per rank and once per node
+    for (int i = tid; i < ntok * a.R; i += kLayoutThreads) {
+        const int tl = i / a.R, r = i - tl * a.R;
+        bool hit = false;
+        for (int j = 0; j < a.k; ++j) {
+            const int e = pair_e[tl * a.k + j];
+            hit |= (e >= 0 && e / a.epr == r);
+        }
+        if (a.in_rank) a.in_rank[(int64_t)(t0 + tl) * a.R + r] = hit ? 1 : 0;
+        if (hit) atomicAdd(&col_agg[a.E + r], 1);
+    }
+    for (int i = tid; i < ntok * a.N; i += kLayoutThreads) {
+        const int tl = i / a.N, n = i - tl * a.N;
+        bool hit = false;
+        for (int j = 0; j < a.k; ++j) {
+            const int e = pair_e[tl * a.k + j];
+            hit |= (e >= 0 && (e / a.epr) / a.rpn == n);
+        }
+        if (hit) atomicAdd(&col_agg[a.E + a.R + n], 1);
+    }
+    __syncthreads();
+
+    // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its prefix)
+    const bool publish = (tile != a.stalled_tile);
+    int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
+    int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
+    for (int c = tid; c < a.cols; c += kLayoutThreads) {
+        if (tile == 0) my_incl[c] = col_agg[c];
+        else my_agg[c] = col_agg[c];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
+
+    // (5) decoupled look-back over earlier tiles
+    if (tile > 0) {
+        int pos = tile - 1;
+        while (true) {
+            if (warp == 0) {
+                const int idx = pos - lane;
+                uint32_t polls = 0;
+                unsigned ns = 32;
+                int win_aggs = 0, win_incl = -1, done = 1;
+                while (true) {
+                    uint32_t st = kStateIncl;  // before tile 0: an empty inclusive prefix
+                    if (idx >= 0) {
+                        const uint32_t v = ld_acquire_gpu(&a.state[idx]);
+                        st = ((v & ~3u) == tag) ? (v & 3u) : 0u;
+                    }
+                    const uint32_t incl_mask = __ballot_sync(0xffffffffu, st == kStateIncl);
+                    const uint32_t wait_mask = __ballot_sync(0xffffffffu, st == 0);
+                    const uint32_t need =
+                        incl_mask ? (((incl_mask & (0u - incl_mask)) << 1) - 1u) : 0xffffffffu;
+                    if ((wait_mask & need) == 0) {
+                        if (incl_mask) {
+                            const int first = __ffs(incl_mask) - 1;
+                            win_aggs = first;
+                            win_incl = pos - first;  // -1 when it is the empty prefix
+                            done = 1;
+                        } else {
+                            win_aggs = 32;
+                            win_incl = -1;
+                            done = 0;
+                        }
+                        break;
+                    }
+                    if (++polls >= a.spin_limit) {
+                        if (lane == 0) report(a.status, EPD_ERR_TIMEOUT);
+                        win_aggs = 0;
+                        win_incl = -1;
+                        done = 1;
+                        break;
+                    }
+                    __nanosleep(ns);
+                    if (ns < 1024) ns <<= 1;
+                }
+                if (lane == 0) {
+                    s_win_aggs = win_aggs;
+                    s_win_incl = win_incl;
+                    s_win_done = done;
+                }
+            }
+            __syncthreads();
+            const int wa = s_win_aggs, wi = s_win_incl, wdone = s_win_done;
+            for (int c = tid; c < a.cols; c += kLayoutThreads) {
+                int sum = 0;
+                for (int l = 0; l < wa; ++l) sum += __ldcg(a.agg + (size_t)(pos - l) * a.cols_pad + c);
+                if (wi >= 0) sum += __ldcg(a.incl + (size_t)wi * a.cols_pad + c);
+                col_excl[c] += sum;
+            }
+            __syncthreads();
+            if (wdone) break;
+            pos -= 32;
+        }
+        // (6) publish the inclusive prefix
+        for (int c = tid; c < a.cols; c += kLayoutThreads) my_incl[c] = col_excl[c] + col_agg[c];
+        __threadfence();
+        __syncthreads();
+        if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | kStateIncl);
+    }
+
+    // (7) rank of every pair inside its expert over the whole batch
+    for (int p = tid; p < npairs; p += kLayoutThreads) {
+        const int e = pair_e[p];
+        const int w = (p >> 5) / cpw;
+        a.pair_rank[pair0 + p] = e >= 0 ? col_excl[e] + hw[w * a.E + e] + pair_r[p] : -1;
+    }
+
+    // (8) the last tile in ticket order holds the totals
+    if (tile == a.tiles - 1) {
+        int part = 0;
+        for (int c = tid; c < a.cols; c += kLayoutThreads) {
+            const int tot = col_excl[c] + col_agg[c];
+            if (c < a.E) {
+                a.per_expert[c] = tot;
+                part += tot;
+            } else if (c < a.E + a.R) {
+                a.per_rank[c - a.E] = tot;
+            } else if (a.per_node) {
+                a.per_node[c - a.E - a.R] = tot;
+            }
+        }
+        part = warp_sum(part);
+        if (lane == 0) s_red[warp] = part;
+        __syncthreads();
+        if (tid == 0) {
+            int P = 0;
+            for (int w = 0; w < kLayoutWarps; ++w) P += s_red[w];
+            a.hdr->total_pairs = P;
+            a.hdr->num_tokens = a.T;
+            a.hdr->num_topk = a.k;
+        }
+    }
+
+    // (9) the last block to finish resets the call state for the next call
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.hdr->done, 1u);
+        if (prev == (unsigned)a.tiles - 1) {
+            a.hdr->done = 0;
+            a.hdr->ticket = 0;
+            a.hdr->epoch = epoch + 1;
+            __threadfence();
+        }
+    }
+}
+
+size_t layout_smem_bytes(int k, int E, int cols_pad) {
+    const int tile = layout_tile_tokens(k);
+    return ((size_t)kLayoutWarps * E + 2 * (size_t)cols_pad + 2 * (size_t)tile * k) * sizeof(int);
+}
+
+constexpr size_t kMaxDynSmem = 227 * 1024;
+
+epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, int N,
+                           int32_t *per_expert, int32_t *per_rank, int32_t *per_node,
+                           uint8_t *in_rank, void *workspace, int32_t *status, int stalled_tile,
+                           uint32_t spin_limit, cudaStream_t stream) {
+    if (!topology_ok(T, k, E, R, N)) return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > 0 && (topk_idx == nullptr || !aligned8(topk_idx))) return EPD_ERR_INVALID_ARG;
+    if (per_expert == nullptr || per_rank == nullptr || status == nullptr || workspace == nullptr)
+        return EPD_ERR_INVALID_ARG;
+    if (!aligned4(per_expert) || !aligned4(per_rank) || !aligned4(status) ||
+        (per_node && !aligned4(per_node)) || !aligned16(workspace))
+        return EPD_ERR_INVALID_ARG;
+    if (spin_limit == 0) return EPD_ERR_INVALID_ARG;
+
+    const WsLayout w = ws_layout(T, k, E, R, N);
+    const size_t smem = layout_smem_bytes(k, E, w.cols_pad);
+    if (smem > kMaxDynSmem) return EPD_ERR_UNSUPPORTED;
+    static size_t smem_opted = 48 * 1024;  // largest dynamic shared memory opted into so far
+    if (smem > smem_opted) {
+        if (cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kMaxDynSmem) != cudaSuccess)
+            return EPD_ERR_CUDA;
+        smem_opted = kMaxDynSmem;
+    }
+
+    char *ws = static_cast<char *>(workspace);
+    LayoutArgs a;
+    a.topk = topk_idx;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.R = R;
+    a.N = N;
+    a.epr = E / R;
+    a.rpn = R / N;
+    a.per_expert = per_expert;
+    a.per_rank = per_rank;
+    a.per_node = per_node;
+    a.in_rank = in_rank;
+    a.hdr = reinterpret_cast<WsHeader *>(ws + w.header_off);
+    a.pair_rank = reinterpret_cast<int32_t *>(ws + w.pair_rank_off);
+    a.state = reinterpret_cast<uint32_t *>(ws + w.state_off);
+    a.agg = reinterpret_cast<int32_t *>(ws + w.agg_off);
+    a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
+    a.tiles = w.tiles;
+    a.tile_tokens = layout_tile_tokens(k);
+    a.cols = w.cols;
+    a.cols_pad = w.cols_pad;
+    a.status = status;
+    a.stalled_tile = stalled_tile;
+    a.spin_limit = spin_limit;
+    layout_kernel<<<w.tiles, kLayoutThreads, smem, stream>>>(a);
+    return launch_status();
+}
+
+}  // namespace
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace epd
+
+extern "C" {
+
+const char *epd_status_string(int code) {
+    switch (code) {
+        case EPD_OK: return "ok";
+        case EPD_ERR_INVALID_ARG: return "invalid argument";
+        case EPD_ERR_UNSUPPORTED: return "unsupported size";
+        case EPD_ERR_CUDA: return "CUDA launch error";
+        case EPD_ERR_INVALID_EXPERT: return "expert id outside [-1, E)";
+        case EPD_ERR_TIMEOUT: return "look-back wait gave up";
+        case EPD_ERR_CAPACITY: return "slot outside the permuted buffer";
+        default: return "unknown status";
+    }
+}
+
+int epd_version(void) { return 10000; }
+
+size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
+                           int num_rdma_ranks) {
+    if (!epd::topology_ok(num_tokens, num_topk, num_experts, num_ranks, num_rdma_ranks)) return 0;
+    return epd::ws_layout(num_tokens, num_topk, num_experts, num_ranks, num_rdma_ranks).total;
+}
+
+epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_stream_t stream) {
+    if (workspace == nullptr || bytes < sizeof(epd::WsHeader)) return EPD_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return EPD_ERR_CUDA;
+    return EPD_OK;
+}
+
+epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                int num_experts, int num_ranks, int num_rdma_ranks,
+                                int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                                int32_t *tokens_per_rdma_rank, uint8_t *is_token_in_rank,
+                                void *workspace, int32_t *status, epd_stream_t stream) {
+    return epd::layout_launch(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
+                              num_rdma_ranks, tokens_per_expert, tokens_per_rank,
+                              tokens_per_rdma_rank, is_token_in_rank, workspace, status, -1,
+                              epd::kDefaultSpinLimit, reinterpret_cast<cudaStream_t>(stream));
+}
+
+epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                          int num_experts, int num_ranks, int num_rdma_ranks,
+                                          int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                                          int32_t *tokens_per_rdma_rank,
+                                          uint8_t *is_token_in_rank, void *workspace,
+                                          int32_t *status, int stalled_tile,
+                                          uint32_t spin_limit, epd_stream_t stream) {
+    if (stalled_tile < 0 || spin_limit > epd::kDefaultSpinLimit) return EPD_ERR_INVALID_ARG;
+    return epd::layout_launch(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
+                              num_rdma_ranks, tokens_per_expert, tokens_per_rank,
+                              tokens_per_rdma_rank, is_token_in_rank, workspace, status,
+                              stalled_tile, spin_limit, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

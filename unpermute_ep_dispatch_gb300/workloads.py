@@ -187,6 +187,11 @@ def make_random_case(T, H, k, E, R, N, dtype="bf16", seed=0, routing="uniform", 
     elif routing == "zipf":
         topk, w, p = route_zipf(g, T, E, k, zipf_s, zero_experts)
         meta["popularity"] = p
+    elif routing == "repeats":          # picks drawn with replacement (an expert may repeat)
+        topk = torch.randint(0, E, (T, k), generator=g, dtype=torch.int64)
+        valid = torch.rand(T, k, generator=g) >= p_invalid
+        topk = torch.where(valid, topk, torch.full_like(topk, -1))
+        w = _masked_softmax(torch.randn(T, k, generator=g), valid)
     elif routing == "invalid":          # every pick dropped
         topk = torch.full((T, k), -1, dtype=torch.int64)
         w = torch.zeros(T, k, dtype=torch.float32)
