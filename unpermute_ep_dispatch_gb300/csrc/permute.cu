@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     const int nwarps = gridDim.x * kWarps;
     for (int t = blockIdx.x * kWarps + warp; t < a.T; t += nwarps) {
         // slots of this token's picks
+        int any = 0;
         for (int j = lane; j < a.k; j += 32) {
             const int64_t idx = (int64_t)t * a.k + j;
             const int64_t e = a.topk[idx];
@@ -72,7 +73,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
             }
             a.output_index[idx] = s;
             s_slot[warp][j] = s;
+            any |= (s >= 0);
         }
+        if (!__any_sync(0xffffffffu, any)) continue;  // no valid pick: nothing to copy
         __syncwarp();
 
         // row: read once, write to every slot
@@ -141,9 +144,9 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
     } else {
         return EPD_ERR_INVALID_ARG;
     }
-    if (!expert_start_loc || !workspace || !m_indices || !output_index || !status)
-        return EPD_ERR_INVALID_ARG;
-    if (T > 0 && (!x || !out || !topk_idx)) return EPD_ERR_INVALID_ARG;
+    if (!expert_start_loc || !workspace || !status) return EPD_ERR_INVALID_ARG;
+    if (capacity_rows > 0 && !m_indices) return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > 0 && (!output_index || !topk_idx || !x || !out)) return EPD_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (out && !aligned16(out)) || (topk_idx && !aligned8(topk_idx)) ||
         !aligned4(expert_start_loc) || !aligned16(workspace) || !aligned4(m_indices) ||
         !aligned4(output_index) || !aligned4(status))
