@@ -20,7 +20,7 @@ def bits16(t: torch.Tensor) -> np.ndarray:
 def row_bytes(t: torch.Tensor) -> np.ndarray:
     """[T, H] tensor of any dtype -> [T, row_bytes] uint8 view of its bytes."""
     t = t.detach().cpu().contiguous()
-    return t.view(torch.uint8).numpy().reshape(t.shape[0], -1)
+    return t.view(torch.uint8).numpy().reshape(t.shape[0], t.shape[1] * t.element_size())
 
 
 def oracle_path(case, capacity=None, topk_override=None):
