@@ -61,7 +61,7 @@ typedef enum {
     EPD_OK = 0,
     EPD_ERR_INVALID_ARG = 1,    /* bad size, null or misaligned pointer, mismatched workspace */
     EPD_ERR_UNSUPPORTED = 2,    /* valid but beyond a documented limit */
-    EPD_ERR_CUDA = 3,           /* a launch failed; cudaGetLastError() has the cause */
+    EPD_ERR_CUDA = 3,           /* a CUDA call failed; epd_last_cuda_error() has the cause */
     EPD_ERR_INVALID_EXPERT = 4, /* (status word) topk_idx held an id outside [-1, E) */
     EPD_ERR_TIMEOUT = 5,        /* (status word) a bounded look-back wait gave up */
     EPD_ERR_CAPACITY = 6,       /* (status word) a slot fell outside [0, capacity_rows) */
@@ -81,6 +81,14 @@ EPD_API const char *epd_status_string(int code);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch. */
 EPD_API int epd_version(void);
+
+/*
+ * The cudaError_t code of the last CUDA failure seen by a libepd call on this
+ * host thread (0 if none). libepd reads and clears the CUDA runtime's
+ * last-error state when a launch fails, so the caller's own error checks are
+ * not disturbed; this is where the cause is kept.
+ */
+EPD_API int epd_last_cuda_error(void);
 
 /*
  * Workspace size in bytes for one layout -> permute chain over T tokens, k

@@ -37,6 +37,7 @@ _P, _I, _I64, _U32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes
 SIGNATURES = {
     "epd_status_string": (ctypes.c_char_p, [_I]),
     "epd_version": (_I, []),
+    "epd_last_cuda_error": (_I, []),
     "epd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "epd_workspace_init": (_I, [_P, _SZ, _P]),
     "ep_dispatch_layout": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
@@ -54,7 +55,10 @@ _lib = None
 class EpdError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        msg = f"{where}: {status_string(code)} (status {code})"
+        if code == EPD_ERR_CUDA:
+            msg += f", cudaError {load_library().epd_last_cuda_error()}"
+        super().__init__(msg)
 
 
 def load_library(path: str = LIB_PATH):

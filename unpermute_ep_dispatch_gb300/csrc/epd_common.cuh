@@ -78,9 +78,12 @@ inline bool topology_ok(int T, int k, int E, int R, int N) {
 
 int sm_count();  // multiprocessors of the current device (cached per device)
 
-inline epd_status_t launch_status() {
-    return cudaGetLastError() == cudaSuccess ? EPD_OK : EPD_ERR_CUDA;
-}
+// Reads and clears the CUDA runtime's last error, keeps its code for
+// epd_last_cuda_error() and maps it to EPD_OK / EPD_ERR_CUDA.
+epd_status_t record_cuda_error();
+int last_cuda_error();
+
+inline epd_status_t launch_status() { return record_cuda_error(); }
 
 // ---------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ void report(int32_t *status, int code) {

@@ -276,8 +276,6 @@ size_t layout_smem_bytes(int k, int E, int cols_pad) {
     return ((size_t)kLayoutWarps * E + 2 * (size_t)cols_pad + 2 * (size_t)tile * k) * sizeof(int);
 }
 
-constexpr size_t kMaxDynSmem = 227 * 1024;
-
 epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, int N,
                            int32_t *per_expert, int32_t *per_rank, int32_t *per_node,
                            uint8_t *in_rank, void *workspace, int32_t *status, int stalled_tile,
@@ -293,13 +291,20 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
 
     const WsLayout w = ws_layout(T, k, E, R, N);
     const size_t smem = layout_smem_bytes(k, E, w.cols_pad);
-    if (smem > kMaxDynSmem) return EPD_ERR_UNSUPPORTED;
-    static size_t smem_opted = 48 * 1024;  // largest dynamic shared memory opted into so far
-    if (smem > smem_opted) {
-        if (cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kMaxDynSmem) != cudaSuccess)
-            return EPD_ERR_CUDA;
-        smem_opted = kMaxDynSmem;
+    if (smem > 48 * 1024) {
+        // the opt-in limit covers static and dynamic shared memory together
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaFuncGetAttributes(&fa, layout_kernel) != cudaSuccess)
+            return record_cuda_error();
+        if (smem + fa.sharedSizeBytes > (size_t)optin) return EPD_ERR_UNSUPPORTED;
+        if ((int)smem > fa.maxDynamicSharedSizeBytes &&
+            cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return record_cuda_error();
     }
 
     char *ws = static_cast<char *>(workspace);
@@ -334,6 +339,18 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
 
 }  // namespace
 
+namespace {
+thread_local int g_last_cuda_error = 0;
+}
+
+int last_cuda_error() { return g_last_cuda_error; }
+
+epd_status_t record_cuda_error() {
+    const cudaError_t e = cudaGetLastError();  // consume it: the caller's runtime state stays clean
+    g_last_cuda_error = (int)e;
+    return e == cudaSuccess ? EPD_OK : EPD_ERR_CUDA;
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -367,6 +384,8 @@ const char *epd_status_string(int code) {
 
 int epd_version(void) { return 10000; }
 
+int epd_last_cuda_error(void) { return epd::last_cuda_error(); }
+
 size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                            int num_rdma_ranks) {
     if (!epd::topology_ok(num_tokens, num_topk, num_experts, num_ranks, num_rdma_ranks)) return 0;
@@ -375,9 +394,8 @@ size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts, int nu
 
 epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_stream_t stream) {
     if (workspace == nullptr || bytes < sizeof(epd::WsHeader)) return EPD_ERR_INVALID_ARG;
-    if (cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return EPD_ERR_CUDA;
-    return EPD_OK;
+    cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream));
+    return epd::record_cuda_error();
 }
 
 epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,

@@ -137,7 +137,9 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
         row_bytes = 2 * (int64_t)H;
         scale_cols = 0;
     } else if (dtype == EPD_FP8_E4M3) {
-        if (H % 128 != 0 || x_scale == nullptr || out_scale == nullptr) return EPD_ERR_INVALID_ARG;
+        if (H % 128 != 0) return EPD_ERR_INVALID_ARG;
+        if (((int64_t)T * k > 0 && x_scale == nullptr) || (capacity_rows > 0 && out_scale == nullptr))
+            return EPD_ERR_INVALID_ARG;
         if (!aligned4(x_scale) || !aligned4(out_scale)) return EPD_ERR_INVALID_ARG;
         row_bytes = H;
         scale_cols = H / 128;
