@@ -189,6 +189,45 @@ EPD_API epd_status_t ep_unpermute(const void *expert_out, int64_t capacity_rows,
                           int num_topk, int hidden, void *y, int32_t *status, epd_stream_t stream);
 
 /*
+ * Allocation-free variant of ep_dispatch_layout. The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory at
+ * the moment they need the layout -- for example code running inside an
+ * inference engine or plugin whose device memory is planned up front and
+ * handed out by the host framework, or code that must not touch the allocator
+ * on a hot serving path. Such callers own the inputs and outputs but have no
+ * way to provide the workspace.
+ *
+ * It computes exactly what ep_dispatch_layout computes (tokens_per_expert,
+ * tokens_per_rank, tokens_per_rdma_rank, is_token_in_rank, same arguments and
+ * errors) but keeps its scratch -- the look-back state and the per-pair ranks --
+ * in a file-scope device array of EPD_NOALLOC_SCRATCH_BYTES (8 MiB) inside
+ * libepd. Every GPU that loads the library holds that array until the process
+ * exits. The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *   - Sizes whose scratch need, epd_workspace_bytes(T, k, E, R, N), exceeds
+ *     EPD_NOALLOC_SCRATCH_BYTES are rejected with EPD_ERR_UNSUPPORTED before
+ *     anything is launched (T*k up to about 1.5 million pairs fits at E = 256).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the previous call's contents;
+ *     each call clears the counters that must start at zero (on `stream`).
+ *     Calls that overlap on the GPU race with each other.
+ *   - The per-pair ranks it leaves in the shared array are not an input to
+ *     ep_permute; a caller running the whole path uses ep_dispatch_layout with
+ *     its own workspace.
+ */
+#define EPD_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+EPD_API epd_status_t ep_dispatch_layout_noalloc(const int64_t *topk_idx, int num_tokens,
+                                                int num_topk, int num_experts, int num_ranks,
+                                                int num_rdma_ranks, int32_t *tokens_per_expert,
+                                                int32_t *tokens_per_rank,
+                                                int32_t *tokens_per_rdma_rank,
+                                                uint8_t *is_token_in_rank, int32_t *status,
+                                                epd_stream_t stream);
+
+/*
  * Test hook for failure detection, not part of the path: runs ep_dispatch_layout
  * with the look-back wait bounded by `spin_limit` polls and with token tile
  * `stalled_tile` never publishing its state, so that every later tile's wait

@@ -44,6 +44,7 @@ SIGNATURES = {
     "ep_scan_offsets": (_I, [_P, _I, _P, _P, _P, _P]),
     "ep_permute": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "ep_unpermute": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "epd_test_layout_stalled_tile": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
                                           _U32, _P]),
 }
@@ -270,6 +271,33 @@ def ep_unpermute(expert_out: torch.Tensor, output_index: torch.Tensor,
                                      T, k, H, _ptr(y), _ptr(status), _stream(stream, dev))
     _check(rc, "ep_unpermute")
     return y
+
+
+def ep_dispatch_layout_noalloc(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
+                               num_rdma_ranks: int, status: torch.Tensor, tokens_per_expert,
+                               tokens_per_rank, tokens_per_rdma_rank=None, is_token_in_rank=None,
+                               stream=None):
+    """ep_dispatch_layout without a caller workspace (its scratch is a fixed
+    device array inside libepd, see epd.h). The caller passes every output
+    tensor; nothing is allocated. Returns the outputs in DeepEP's order."""
+    _want(topk_idx, "topk_idx", torch.int64)
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [num_tokens, num_topk]")
+    dev = topk_idx.device
+    T, k = topk_idx.shape
+    E, R, N = int(num_experts), int(num_ranks), int(num_rdma_ranks)
+    _want(status, "status", torch.int32, (1,), dev)
+    _want(tokens_per_expert, "tokens_per_expert", torch.int32, (E,), dev)
+    _want(tokens_per_rank, "tokens_per_rank", torch.int32, (R,), dev)
+    if tokens_per_rdma_rank is not None:
+        _want(tokens_per_rdma_rank, "tokens_per_rdma_rank", torch.int32, (N,), dev)
+    if is_token_in_rank is not None:
+        _want(is_token_in_rank, "is_token_in_rank", torch.bool, (T, R), dev)
+    rc = load_library().ep_dispatch_layout_noalloc(
+        _ptr(topk_idx), T, k, E, R, N, _ptr(tokens_per_expert), _ptr(tokens_per_rank),
+        _ptr(tokens_per_rdma_rank), _ptr(is_token_in_rank), _ptr(status), _stream(stream, dev))
+    _check(rc, "ep_dispatch_layout_noalloc")
+    return tokens_per_rank, tokens_per_rdma_rank, tokens_per_expert, is_token_in_rank
 
 
 def epd_test_layout_stalled_tile(topk_idx, num_experts, num_ranks, num_rdma_ranks, workspace,

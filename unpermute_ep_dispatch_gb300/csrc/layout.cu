@@ -24,6 +24,9 @@
 // Every value is an integer sum, so the outputs are the same whichever order
 // the blocks run in. Waits are bounded: a wait that runs out sets
 // EPD_ERR_TIMEOUT and the block carries on.
+#include <atomic>
+#include <cstddef>
+
 #include "epd_common.cuh"
 
 namespace epd {
@@ -424,3 +427,64 @@ epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_token
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------- allocation-free variant
+// Scratch for ep_dispatch_layout_noalloc: a file-scope device array that every
+// GPU loading this library holds until the process exits. Host code must not
+// pass `g_noalloc_scratch` itself to a kernel (on the host it names a host-side
+// stand-in); it passes the device address resolved by cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EPD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<void *> g_noalloc_addr[kMaxDevices];
+
+// Device address of the scratch on the current device, resolved once per device.
+epd_status_t noalloc_scratch_address(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return epd::record_cuda_error();
+    if (dev < 0 || dev >= kMaxDevices) return EPD_ERR_UNSUPPORTED;
+    void *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            epd::record_cuda_error();
+            return EPD_ERR_CUDA;
+        }
+        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+    *addr = p;
+    return EPD_OK;
+}
+
+}  // namespace
+
+extern "C" epd_status_t ep_dispatch_layout_noalloc(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                        int num_experts, int num_ranks, int num_rdma_ranks,
+                                        int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                                        int32_t *tokens_per_rdma_rank,
+                                        uint8_t *is_token_in_rank, int32_t *status,
+                                        epd_stream_t stream) {
+    using namespace epd;
+    const int T = num_tokens, k = num_topk;
+    if (!topology_ok(T, k, num_experts, num_ranks, num_rdma_ranks)) return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > 0 && (topk_idx == nullptr || !aligned8(topk_idx))) return EPD_ERR_INVALID_ARG;
+    if (!tokens_per_expert || !tokens_per_rank || !status || !aligned4(tokens_per_expert) ||
+        !aligned4(tokens_per_rank) || !aligned4(status) ||
+        (tokens_per_rdma_rank && !aligned4(tokens_per_rdma_rank)))
+        return EPD_ERR_INVALID_ARG;
+    if (ws_layout(T, k, num_experts, num_ranks, num_rdma_ranks).total > EPD_NOALLOC_SCRATCH_BYTES)
+        return EPD_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    const epd_status_t st = noalloc_scratch_address(&scratch);
+    if (st != EPD_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The tile ticket and the finished-block count must start at zero; the call
+    // counter that tags the look-back state carries over from the previous call.
+    if (cudaMemsetAsync(scratch, 0, offsetof(WsHeader, epoch), s) != cudaSuccess)
+        return record_cuda_error();
+    return layout_launch(topk_idx, T, k, num_experts, num_ranks, num_rdma_ranks,
+                         tokens_per_expert, tokens_per_rank, tokens_per_rdma_rank,
+                         is_token_in_rank, scratch, status, -1, kDefaultSpinLimit, s);
+}
+
