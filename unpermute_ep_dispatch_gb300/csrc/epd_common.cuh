@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "epd.h"
 
 namespace epd {
@@ -85,9 +87,52 @@ int last_cuda_error();
 
 inline epd_status_t launch_status() { return record_cuda_error(); }
 
+// Launch with programmatic dependent launch: the kernel may be scheduled while
+// the previous kernel on the stream drains, and waits (griddepcontrol.wait)
+// before it touches memory that kernel wrote. Hides the launch gap between the
+// four steps of the path.
+template <typename... KArgs, typename... Args>
+inline epd_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                               cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return record_cuda_error();
+}
+
+// Resident blocks of `kernel` per SM at `block` threads and `smem` dynamic bytes.
+template <typename K>
+inline int blocks_per_sm(K kernel, int block, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess ||
+        n < 1) {
+        cudaGetLastError();
+        n = 1;
+    }
+    return n;
+}
+
 // ---------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ void report(int32_t *status, int code) {
     atomicCAS(status, 0, code);
+}
+
+// Wait until the previous kernel on the stream has completed and its writes
+// are visible (a no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel on the stream to be scheduled (it still waits for this
+// one to complete before reading what this one writes).
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -115,7 +160,7 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
 // Streaming 16-byte load that does not allocate in L1 (each row is read once).
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;

@@ -59,25 +59,30 @@ __device__ __forceinline__ int warp_sum(int v) {
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     extern __shared__ int4 smem_raw[];
-    int *hw = reinterpret_cast<int *>(smem_raw);           // [warps][E] histograms -> warp bases
+    const int tile_pairs = a.tile_tokens * a.k;
+    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);  // [tile tokens]
+    int *hw = reinterpret_cast<int *>(tok_rmask + a.tile_tokens);  // [warps][E] histograms -> bases
     int *col_agg = hw + kLayoutWarps * a.E;                // [cols_pad] this tile's counts
     int *col_excl = col_agg + a.cols_pad;                  // [cols_pad] counts of earlier tiles
     int *pair_e = col_excl + a.cols_pad;                   // [tile pairs] expert or -1
-    int *pair_r = pair_e + a.tile_tokens * a.k;            // [tile pairs] rank inside the warp
+    int *pair_r = pair_e + tile_pairs;                     // [tile pairs] rank inside the warp
+    int *pair_rk = pair_r + tile_pairs;                    // [tile pairs] simulated rank or -1
     __shared__ int s_tile;
     __shared__ uint32_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
     __shared__ int s_red[kLayoutWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        s_tile = (int)atomicAdd(&a.hdr->ticket, 1u);
-        s_epoch = ld_relaxed_gpu(&a.hdr->epoch);
-    }
     for (int i = tid; i < kLayoutWarps * a.E; i += kLayoutThreads) hw[i] = 0;
     for (int i = tid; i < a.cols_pad; i += kLayoutThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
+    }
+    pdl_wait();  // the workspace and topk_idx may come from the previous kernel
+    pdl_trigger();
+    if (tid == 0) {
+        s_tile = (int)atomicAdd(&a.hdr->ticket, 1u);
+        s_epoch = ld_relaxed_gpu(&a.hdr->epoch);
     }
     __syncthreads();
     const int tile = s_tile;
@@ -101,6 +106,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
             if (v >= 0 && v < a.E) e = (int)v;
             else if (v != -1) report(a.status, EPD_ERR_INVALID_EXPERT);
             pair_e[p] = e;
+            pair_rk[p] = e >= 0 ? e / a.epr : -1;
         }
         const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
         if (e >= 0) {
@@ -126,25 +132,32 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
         }
         col_agg[e] = run;
     }
-    // (3) ranks and nodes: a token counts once per rank and once per node
-    for (int i = tid; i < ntok * a.R; i += kLayoutThreads) {
-        const int tl = i / a.R, r = i - tl * a.R;
-        bool hit = false;
+    // (3) ranks and nodes touched by each token: a token counts once per rank / node
+    const bool small_r = a.R <= 64, small_n = a.N <= 64;
+    for (int tl = tid; tl < ntok; tl += kLayoutThreads) {
+        const int *pr = pair_rk + tl * a.k;
+        unsigned long long rm = 0, nm = 0;
         for (int j = 0; j < a.k; ++j) {
-            const int e = pair_e[tl * a.k + j];
-            hit |= (e >= 0 && e / a.epr == r);
+            const int r = pr[j];
+            if (r < 0) continue;
+            const int n = r / a.rpn;
+            bool new_r = true, new_n = true;
+            if (small_r) {
+                new_r = !((rm >> r) & 1ull);
+                rm |= 1ull << r;
+            } else {
+                for (int j2 = 0; j2 < j && new_r; ++j2) new_r = pr[j2] != r;
+            }
+            if (small_n) {
+                new_n = !((nm >> n) & 1ull);
+                nm |= 1ull << n;
+            } else {
+                for (int j2 = 0; j2 < j && new_n; ++j2) new_n = !(pr[j2] >= 0 && pr[j2] / a.rpn == n);
+            }
+            if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+            if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
         }
-        if (a.in_rank) a.in_rank[(int64_t)(t0 + tl) * a.R + r] = hit ? 1 : 0;
-        if (hit) atomicAdd(&col_agg[a.E + r], 1);
-    }
-    for (int i = tid; i < ntok * a.N; i += kLayoutThreads) {
-        const int tl = i / a.N, n = i - tl * a.N;
-        bool hit = false;
-        for (int j = 0; j < a.k; ++j) {
-            const int e = pair_e[tl * a.k + j];
-            hit |= (e >= 0 && (e / a.epr) / a.rpn == n);
-        }
-        if (hit) atomicAdd(&col_agg[a.E + a.R + n], 1);
+        tok_rmask[tl] = rm;
     }
     __syncthreads();
 
@@ -159,6 +172,21 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     __threadfence();
     __syncthreads();
     if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
+
+    // is_token_in_rank rows of this tile (nothing waits on them)
+    if (a.in_rank) {
+        uint8_t *rows = a.in_rank + (int64_t)t0 * a.R;
+        for (int i = tid; i < ntok * a.R; i += kLayoutThreads) {
+            const int tl = i / a.R, r = i - tl * a.R;
+            bool hit = false;
+            if (small_r) {
+                hit = (tok_rmask[tl] >> r) & 1ull;
+            } else {
+                for (int j = 0; j < a.k; ++j) hit |= pair_rk[tl * a.k + j] == r;
+            }
+            rows[i] = hit ? 1 : 0;
+        }
+    }
 
     // (5) decoupled look-back over earlier tiles
     if (tile > 0) {
@@ -183,7 +211,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
                         if (incl_mask) {
                             const int first = __ffs(incl_mask) - 1;
                             win_aggs = first;
-                            win_incl = pos - first;  // -1 when it is the empty prefix
+                            win_incl = pos - first;  // negative when it is the empty prefix
                             done = 1;
                         } else {
                             win_aggs = 32;
@@ -211,8 +239,12 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
             __syncthreads();
             const int wa = s_win_aggs, wi = s_win_incl, wdone = s_win_done;
             for (int c = tid; c < a.cols; c += kLayoutThreads) {
+                // all window rows are loaded at once: one L2 round trip, not one per row
+                const int32_t *col = a.agg + (size_t)pos * a.cols_pad + c;
                 int sum = 0;
-                for (int l = 0; l < wa; ++l) sum += __ldcg(a.agg + (size_t)(pos - l) * a.cols_pad + c);
+#pragma unroll
+                for (int l = 0; l < 32; ++l)
+                    if (l < wa) sum += __ldcg(col - (size_t)l * a.cols_pad);
                 if (wi >= 0) sum += __ldcg(a.incl + (size_t)wi * a.cols_pad + c);
                 col_excl[c] += sum;
             }
@@ -276,7 +308,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
 
 size_t layout_smem_bytes(int k, int E, int cols_pad) {
     const int tile = layout_tile_tokens(k);
-    return ((size_t)kLayoutWarps * E + 2 * (size_t)cols_pad + 2 * (size_t)tile * k) * sizeof(int);
+    return (size_t)tile * sizeof(unsigned long long) +
+           ((size_t)kLayoutWarps * E + 2 * (size_t)cols_pad + 3 * (size_t)tile * k) * sizeof(int);
 }
 
 epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, int N,
@@ -336,8 +369,7 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.status = status;
     a.stalled_tile = stalled_tile;
     a.spin_limit = spin_limit;
-    layout_kernel<<<w.tiles, kLayoutThreads, smem, stream>>>(a);
-    return launch_status();
+    return launch_pdl(layout_kernel, w.tiles, kLayoutThreads, smem, stream, a);
 }
 
 }  // namespace

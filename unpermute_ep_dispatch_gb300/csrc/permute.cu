@@ -8,11 +8,12 @@
 //
 // The slot of pair (t, j) with expert e is expert_start_loc[e] plus the pair's
 // rank inside e, which the layout kernel left in the workspace, so every token
-// is independent: one warp per token, a grid sized to fill the GPU, no
-// cross-block dependency and the same cost per token whatever the routing skew.
-// The row is read once (16-byte streaming loads that bypass L1) and written k
-// times with 16-byte coalesced stores: each warp-wide store covers 512
-// contiguous bytes of a destination row.
+// is independent and the cost per token does not depend on the routing skew.
+// The work is cut into units of (token, 1 KiB of its row) and a persistent grid
+// (resident blocks x SMs) gives every warp an equal contiguous run of units, so
+// no SM idles in a tail wave. Each unit is read once (16-byte streaming loads
+// that bypass L1) and written k times with 16-byte coalesced stores: every
+// warp-wide store covers 512 contiguous bytes of a destination row.
 #include "epd_common.cuh"
 
 namespace epd {
@@ -20,7 +21,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 8;  // 16-byte vectors per lane in flight per pass
+constexpr int kUnitVecs = 64;  // 16-byte vectors per work unit (1 KiB of a row)
 
 struct PermuteArgs {
     const uint8_t *x;
@@ -44,6 +45,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     __shared__ int s_slot[kWarps][EPD_MAX_TOPK];
     __shared__ int s_ok, s_P;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();  // offsets and pair ranks come from the previous kernels
+    pdl_trigger();
     if (threadIdx.x == 0) {
         const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
         s_ok = ok;
@@ -54,59 +57,62 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     if (!s_ok) return;
 
     const int64_t row_vecs = a.row_bytes >> 4;
-    const int nwarps = gridDim.x * kWarps;
-    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += nwarps) {
-        // slots of this token's picks
-        int any = 0;
-        for (int j = lane; j < a.k; j += 32) {
-            const int64_t idx = (int64_t)t * a.k + j;
-            const int64_t e = a.topk[idx];
-            int s = -1;
-            if (e >= 0 && e < a.E) {
-                const int64_t sl = (int64_t)a.start[e] + a.pair_rank[idx];
-                if (sl >= 0 && sl < a.capacity) {
-                    s = (int)sl;
-                    a.m_indices[s] = (int)e;
-                } else {
-                    report(a.status, EPD_ERR_CAPACITY);
+    const int upt = (int)((row_vecs + kUnitVecs - 1) / kUnitVecs);  // units per token
+    const int64_t units = (int64_t)a.T * upt;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t u_end = units * (gw + 1) / nw;
+    int cur_t = -1;
+    bool any = false;
+    for (int64_t u = units * gw / nw; u < u_end; ++u) {
+        const int t = (int)(u / upt);
+        const int ch = (int)(u - (int64_t)t * upt);
+        if (t != cur_t) {
+            // slots of this token's picks; the unit holding chunk 0 records them
+            cur_t = t;
+            int has = 0;
+            __syncwarp();
+            for (int j = lane; j < a.k; j += 32) {
+                const int64_t idx = (int64_t)t * a.k + j;
+                const int64_t e = a.topk[idx];
+                int s = -1;
+                if (e >= 0 && e < a.E) {
+                    const int64_t sl = (int64_t)a.start[e] + a.pair_rank[idx];
+                    if (sl >= 0 && sl < a.capacity) s = (int)sl;
+                    else if (ch == 0) report(a.status, EPD_ERR_CAPACITY);
                 }
+                if (ch == 0) {
+                    a.output_index[idx] = s;
+                    if (s >= 0) a.m_indices[s] = (int)e;
+                }
+                s_slot[warp][j] = s;
+                has |= (s >= 0);
             }
-            a.output_index[idx] = s;
-            s_slot[warp][j] = s;
-            any |= (s >= 0);
+            any = __any_sync(0xffffffffu, has);
+            __syncwarp();
         }
-        if (!__any_sync(0xffffffffu, any)) continue;  // no valid pick: nothing to copy
-        __syncwarp();
+        if (!any) continue;  // no valid pick: nothing to copy
 
-        // row: read once, write to every slot
         const uint8_t *src = a.x + (int64_t)t * a.row_bytes;
-        for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * kUnroll) {
-            uint4 v[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t c = c0 + u * 32 + lane;
-                v[u] = c < row_vecs ? ld_stream16(src + (c << 4)) : make_uint4(0, 0, 0, 0);
-            }
-            for (int j = 0; j < a.k; ++j) {
-                const int s = s_slot[warp][j];
-                if (s < 0) continue;
-                uint8_t *dst = a.out + (int64_t)s * a.row_bytes;
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int64_t c = c0 + u * 32 + lane;
-                    if (c < row_vecs) st16(dst + (c << 4), v[u]);
+        const int64_t c0 = (int64_t)ch * kUnitVecs + lane, c1 = c0 + 32;
+        const uint4 v0 = c0 < row_vecs ? ld_stream16(src + (c0 << 4)) : make_uint4(0, 0, 0, 0);
+        const uint4 v1 = c1 < row_vecs ? ld_stream16(src + (c1 << 4)) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < a.k; ++j) {
+            const int s = s_slot[warp][j];
+            if (s < 0) continue;
+            uint8_t *dst = a.out + (int64_t)s * a.row_bytes;
+            if (c0 < row_vecs) st16(dst + (c0 << 4), v0);
+            if (c1 < row_vecs) st16(dst + (c1 << 4), v1);
+        }
+        if (ch == 0) {  // fp8 scale row travels with chunk 0
+            for (int c = lane; c < a.scale_cols; c += 32) {
+                const float sv = a.x_scale[(int64_t)t * a.scale_cols + c];
+                for (int j = 0; j < a.k; ++j) {
+                    const int s = s_slot[warp][j];
+                    if (s >= 0) a.out_scale[(int64_t)s * a.scale_cols + c] = sv;
                 }
             }
         }
-        // fp8 scale row
-        for (int c = lane; c < a.scale_cols; c += 32) {
-            const float sv = a.x_scale[(int64_t)t * a.scale_cols + c];
-            for (int j = 0; j < a.k; ++j) {
-                const int s = s_slot[warp][j];
-                if (s >= 0) a.out_scale[(int64_t)s * a.scale_cols + c] = sv;
-            }
-        }
-        __syncwarp();
     }
 
     // rows [P, capacity) hold no pair
@@ -174,9 +180,11 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
     a.output_index = output_index;
     a.status = status;
 
-    const int64_t want = ((int64_t)T + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    const int grid = (int)(want < 1 ? 1 : (want < cap ? want : cap));
-    permute_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return launch_status();
+    static int resident = 0;
+    if (resident == 0) resident = blocks_per_sm(permute_kernel, kThreads, 0);
+    const int64_t units = (int64_t)T * ((row_bytes / 16 + kUnitVecs - 1) / kUnitVecs);
+    const int64_t want = (units + kWarps - 1) / kWarps;
+    const int64_t full = (int64_t)sm_count() * resident;
+    const int grid = (int)(want < 1 ? 1 : (want < full ? want : full));
+    return launch_pdl(permute_kernel, grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream), a);
 }

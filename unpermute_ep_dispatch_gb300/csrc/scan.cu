@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kScanThreads)
                 int32_t *__restrict__ total, int32_t *status) {
     __shared__ int s_warp[kScanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();  // the counts come from the layout kernel
+    pdl_trigger();
     int v[kScanItems];
     int sum = 0;
 #pragma unroll
@@ -78,7 +80,6 @@ extern "C" epd_status_t ep_scan_offsets(const int32_t *tokens_per_expert, int nu
     if (!aligned4(tokens_per_expert) || !aligned4(expert_start_loc) || !aligned4(total_rows) ||
         !aligned4(status))
         return EPD_ERR_INVALID_ARG;
-    scan_kernel<<<1, kScanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tokens_per_expert, num_experts, expert_start_loc, total_rows, status);
-    return launch_status();
+    return launch_pdl(scan_kernel, 1, kScanThreads, 0, reinterpret_cast<cudaStream_t>(stream),
+                      tokens_per_expert, num_experts, expert_start_loc, total_rows, status);
 }

@@ -7,11 +7,12 @@
 // with each product and each sum rounded to fp32 (no fused multiply-add) and
 // one round-to-nearest-even at the end.
 //
-// One warp per token. Each lane owns 16-byte column chunks (8 bf16 values);
-// for a group of KT picks it issues all KT x U row loads before any arithmetic,
-// so a resident warp keeps KT * U * 512 bytes of gathers in flight. Loads
-// bypass L1 (each expert-output row is read exactly once); y is written with
-// 16-byte coalesced stores.
+// The work is cut into units of (token, 32*U 16-byte column chunks) and a
+// persistent grid (resident blocks x SMs) gives every warp an equal contiguous
+// run of units. For a group of KT picks a lane issues all KT x U row loads
+// before any arithmetic, so each warp keeps KT * U * 512 bytes of gathers in
+// flight. Loads bypass L1 (each expert-output row is read exactly once); y is
+// written with 16-byte coalesced stores.
 #include <cuda_bf16.h>
 
 #include "epd_common.cuh"
@@ -58,70 +59,88 @@ __global__ void __launch_bounds__(kThreads) unpermute_kernel(UnpermuteArgs a) {
     __shared__ int s_slot[kWarps][EPD_MAX_TOPK];
     __shared__ float s_w[kWarps][EPD_MAX_TOPK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = gridDim.x * kWarps;
+    pdl_wait();  // output_index (and the expert outputs) come from earlier kernels
+    pdl_trigger();
     const int64_t row_bytes = a.row_vecs << 4;
-    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += nwarps) {
-        for (int j = lane; j < a.k; j += 32) {
-            const int64_t idx = (int64_t)t * a.k + j;
-            int s = a.output_index[idx];
-            if (s < -1 || (int64_t)s >= a.capacity) {
-                report(a.status, EPD_ERR_CAPACITY);
-                s = -1;
+    constexpr int kUnitVecs = 32 * U;
+    const int upt = (int)((a.row_vecs + kUnitVecs - 1) / kUnitVecs);  // units per token
+    const int64_t units = (int64_t)a.T * upt;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t u_end = units * (gw + 1) / nw;
+    int cur_t = -1;
+    for (int64_t u = units * gw / nw; u < u_end; ++u) {
+        const int t = (int)(u / upt);
+        const int ch = (int)(u - (int64_t)t * upt);
+        if (t != cur_t) {
+            cur_t = t;
+            __syncwarp();
+            for (int j = lane; j < a.k; j += 32) {
+                const int64_t idx = (int64_t)t * a.k + j;
+                int s = a.output_index[idx];
+                if (s < -1 || (int64_t)s >= a.capacity) {
+                    if (ch == 0) report(a.status, EPD_ERR_CAPACITY);
+                    s = -1;
+                }
+                s_slot[warp][j] = s;
+                s_w[warp][j] = a.w[idx];
             }
-            s_slot[warp][j] = s;
-            s_w[warp][j] = a.w[idx];
+            __syncwarp();
         }
-        __syncwarp();
+        const int64_t c0 = (int64_t)ch * kUnitVecs + lane;
+        float acc[U][8];
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[uu][i] = 0.0f;
+        for (int jg = 0; jg < a.k; jg += KT) {
+            uint4 v[KT][U];
+#pragma unroll
+            for (int jj = 0; jj < KT; ++jj) {
+                const int j = jg + jj;
+                const int s = j < a.k ? s_slot[warp][j] : -1;
+                const uint8_t *src = a.eo + (int64_t)(s < 0 ? 0 : s) * row_bytes;
+#pragma unroll
+                for (int uu = 0; uu < U; ++uu) {
+                    const int64_t c = c0 + uu * 32;
+                    v[jj][uu] = (s >= 0 && c < a.row_vecs) ? ld_stream16(src + (c << 4))
+                                                           : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < KT; ++jj) {
+                const int j = jg + jj;
+                if (j >= a.k || s_slot[warp][j] < 0) continue;
+                const float wj = s_w[warp][j];
+#pragma unroll
+                for (int uu = 0; uu < U; ++uu) accum8(acc[uu], wj, v[jj][uu]);
+            }
+        }
         uint8_t *dst = a.y + (int64_t)t * row_bytes;
-        for (int64_t c0 = 0; c0 < a.row_vecs; c0 += 32 * U) {
-            float acc[U][8];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-            for (int jg = 0; jg < a.k; jg += KT) {
-                uint4 v[KT][U];
-#pragma unroll
-                for (int jj = 0; jj < KT; ++jj) {
-                    const int j = jg + jj;
-                    const int s = j < a.k ? s_slot[warp][j] : -1;
-                    const uint8_t *src = a.eo + (int64_t)(s < 0 ? 0 : s) * row_bytes;
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int64_t c = c0 + u * 32 + lane;
-                        v[jj][u] = (s >= 0 && c < a.row_vecs) ? ld_stream16(src + (c << 4))
-                                                              : make_uint4(0, 0, 0, 0);
-                    }
-                }
-#pragma unroll
-                for (int jj = 0; jj < KT; ++jj) {
-                    const int j = jg + jj;
-                    if (j >= a.k || s_slot[warp][j] < 0) continue;
-                    const float wj = s_w[warp][j];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) accum8(acc[u], wj, v[jj][u]);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + u * 32 + lane;
-                if (c < a.row_vecs) {
-                    uint4 o;
-                    o.x = pack_bf16(acc[u][0], acc[u][1]);
-                    o.y = pack_bf16(acc[u][2], acc[u][3]);
-                    o.z = pack_bf16(acc[u][4], acc[u][5]);
-                    o.w = pack_bf16(acc[u][6], acc[u][7]);
-                    st16(dst + (c << 4), o);
-                }
+        for (int uu = 0; uu < U; ++uu) {
+            const int64_t c = c0 + uu * 32;
+            if (c < a.row_vecs) {
+                uint4 o;
+                o.x = pack_bf16(acc[uu][0], acc[uu][1]);
+                o.y = pack_bf16(acc[uu][2], acc[uu][3]);
+                o.z = pack_bf16(acc[uu][4], acc[uu][5]);
+                o.w = pack_bf16(acc[uu][6], acc[uu][7]);
+                st16(dst + (c << 4), o);
             }
         }
-        __syncwarp();
     }
 }
 
 template <int KT, int U>
-void launch(const UnpermuteArgs &a, int grid, cudaStream_t stream) {
-    unpermute_kernel<KT, U><<<grid, kThreads, 0, stream>>>(a);
+epd_status_t launch(const UnpermuteArgs &a, cudaStream_t stream) {
+    static int resident = 0;
+    if (resident == 0) resident = blocks_per_sm(unpermute_kernel<KT, U>, kThreads, 0);
+    const int64_t units = (int64_t)a.T * ((a.row_vecs + 32 * U - 1) / (32 * U));
+    const int64_t want = (units + kWarps - 1) / kWarps;
+    const int64_t full = (int64_t)sm_count() * resident;
+    const int grid = (int)(want < 1 ? 1 : (want < full ? want : full));
+    return launch_pdl(unpermute_kernel<KT, U>, grid, kThreads, 0, stream, a);
 }
 
 }  // namespace
@@ -154,13 +173,9 @@ extern "C" epd_status_t ep_unpermute(const void *expert_out, int64_t capacity_ro
     a.row_vecs = H / 8;
     a.y = static_cast<uint8_t *>(y);
     a.status = status;
-    const int64_t want = ((int64_t)T + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    const int grid = (int)(want < cap ? want : cap);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (k <= 1) launch<1, 8>(a, grid, s);
-    else if (k <= 2) launch<2, 4>(a, grid, s);
-    else if (k <= 4) launch<4, 4>(a, grid, s);
-    else launch<8, 2>(a, grid, s);
-    return launch_status();
+    if (k <= 1) return launch<1, 4>(a, s);
+    if (k <= 2) return launch<2, 4>(a, s);
+    if (k <= 4) return launch<4, 2>(a, s);
+    return launch<8, 2>(a, s);
 }
