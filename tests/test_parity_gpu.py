@@ -219,3 +219,27 @@ def test_binding_validates_tensors():
         epd.ep_dispatch_layout(g.topk, 16, 3, 1, g.ws, g.status)
     with pytest.raises(ValueError):
         epd.ep_unpermute(g.out.float(), g.output_index, g.w, g.status)
+
+
+def test_cuda_graph_replay_of_the_step():
+    """One step captured in a CUDA graph, replayed on fresh inputs copied into the
+    captured buffers (the decode pattern): every replay matches the oracle."""
+    cases = [workloads.make_case("decode_fp8", seed=2000 + i) for i in range(3)]
+    g = GpuPath(cases[0])
+    g.step()                                     # warm: library loaded, attributes set
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g.stream = s
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.step()
+    for case in cases:
+        g.case = case
+        g.topk.copy_(case.topk_idx)
+        g.w.copy_(case.topk_weights)
+        g.x.copy_(case.x)
+        g.xs.copy_(case.x_scale)
+        g.eo.copy_(case.expert_out)
+        torch.cuda.synchronize()
+        graph.replay()
+        compare(g.results(), oracle_path(case))

@@ -28,18 +28,21 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 64, "header is one 64-byte block");
 
 constexpr size_t kAlign = 256;
-constexpr int kLayoutThreads = 256;
-constexpr int kLayoutWarps = kLayoutThreads / 32;
-constexpr int kMaxPairsPerTile = 512;
+constexpr int kLayoutChunks = 8;                       // 32-pair chunks per layout warp
+constexpr int kLayoutPairsPerWarp = 32 * kLayoutChunks;
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Tokens per layout tile: at most 512 (token, pick) pairs and at most 256 tokens.
-__host__ __device__ inline int layout_tile_tokens(int k) {
-    int t = k > 0 ? kMaxPairsPerTile / k : 256;
-    if (t < 1) t = 1;
-    if (t > 256) t = 256;
-    return t;
+// Warps per layout block: each warp keeps a private E-wide histogram in shared
+// memory, so fewer warps for larger E (at most 64 KiB of histograms).
+__host__ __device__ inline int layout_warps(int E) {
+    return E <= 512 ? 32 : E <= 1024 ? 16 : E <= 2048 ? 8 : 4;
+}
+
+// Tokens per layout tile: the tile holds at most 256 (token, pick) pairs per warp.
+__host__ __device__ inline int layout_tile_tokens(int k, int E) {
+    const int pairs = kLayoutPairsPerWarp * layout_warps(E);
+    return k > 0 ? pairs / k : pairs;
 }
 
 struct WsLayout {
@@ -51,7 +54,7 @@ __host__ __device__ inline size_t ws_pair_rank_off() { return kAlign; }
 
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N) {
     WsLayout w;
-    int tile = layout_tile_tokens(k);
+    int tile = layout_tile_tokens(k, E);
     w.tiles = T > 0 ? (T + tile - 1) / tile : 1;
     w.cols = E + R + N;
     w.cols_pad = (int)align_up((size_t)w.cols, 32);

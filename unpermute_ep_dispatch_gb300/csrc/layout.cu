@@ -57,24 +57,21 @@ __device__ __forceinline__ int warp_sum(int v) {
     return v;
 }
 
-__global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
+template <int W>
+__global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
+    constexpr int kThreads = W * 32;
     extern __shared__ int4 smem_raw[];
-    const int tile_pairs = a.tile_tokens * a.k;
-    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);  // [tile tokens]
-    int *hw = reinterpret_cast<int *>(tok_rmask + a.tile_tokens);  // [warps][E] histograms -> bases
-    int *col_agg = hw + kLayoutWarps * a.E;                // [cols_pad] this tile's counts
-    int *col_excl = col_agg + a.cols_pad;                  // [cols_pad] counts of earlier tiles
-    int *pair_e = col_excl + a.cols_pad;                   // [tile pairs] expert or -1
-    int *pair_r = pair_e + tile_pairs;                     // [tile pairs] rank inside the warp
-    int *pair_rk = pair_r + tile_pairs;                    // [tile pairs] simulated rank or -1
+    int *hw = reinterpret_cast<int *>(smem_raw);  // [W][E] warp histograms -> warp bases
+    int *col_agg = hw + W * a.E;                   // [cols_pad] this tile's counts
+    int *col_excl = col_agg + a.cols_pad;          // [cols_pad] counts of earlier tiles
     __shared__ int s_tile;
     __shared__ uint32_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
-    __shared__ int s_red[kLayoutWarps];
+    __shared__ int s_red[W];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < kLayoutWarps * a.E; i += kLayoutThreads) hw[i] = 0;
-    for (int i = tid; i < a.cols_pad; i += kLayoutThreads) {
+    for (int i = tid; i < W * a.E; i += kThreads) hw[i] = 0;
+    for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
     }
@@ -93,27 +90,31 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     const int npairs = ntok * a.k;
     const int64_t pair0 = (int64_t)t0 * a.k;
 
-    // (1) warp-aggregated histograms over contiguous runs of 32-pair chunks
-    const int nchunks = (npairs + 31) >> 5;
-    const int cpw = (nchunks + kLayoutWarps - 1) / kLayoutWarps;
+    // (1) warp w owns pairs [256 w, 256 w + 256) of the tile, in row-major order.
+    // All of a lane's picks are loaded at once, then each 32-pair chunk is ranked:
+    // lanes holding the same expert find each other with __match_any_sync and the
+    // lowest of them adds the group's size to the warp's private histogram.
+    int pe[kLayoutChunks], pr[kLayoutChunks];
+    const int p_base = warp * kLayoutPairsPerWarp + lane;
+#pragma unroll
+    for (int c = 0; c < kLayoutChunks; ++c) {
+        const int p = p_base + 32 * c;
+        int64_t v = -1;
+        if (p < npairs) v = __ldg(a.topk + pair0 + p);
+        pe[c] = (v >= 0 && v < a.E) ? (int)v : -1;
+        if (v < -1 || v >= a.E) report(a.status, EPD_ERR_INVALID_EXPERT);
+    }
     int *my_hist = hw + warp * a.E;
-    const int c_end = min(nchunks, (warp + 1) * cpw);
-    for (int c = warp * cpw; c < c_end; ++c) {
-        const int p = (c << 5) + lane;
-        int e = -1;
-        if (p < npairs) {
-            const int64_t v = a.topk[pair0 + p];
-            if (v >= 0 && v < a.E) e = (int)v;
-            else if (v != -1) report(a.status, EPD_ERR_INVALID_EXPERT);
-            pair_e[p] = e;
-            pair_rk[p] = e >= 0 ? e / a.epr : -1;
-        }
+#pragma unroll
+    for (int c = 0; c < kLayoutChunks; ++c) {
+        const int e = pe[c];
         const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
+        pr[c] = 0;
         if (e >= 0) {
             const uint32_t peers = __match_any_sync(valid, e);
             const int before = __popc(peers & lanemask_lt());
             const int base = my_hist[e];
-            pair_r[p] = base + before;
+            pr[c] = base + before;
             __syncwarp(peers);
             if (before == 0) my_hist[e] = base + __popc(peers);
         }
@@ -122,42 +123,66 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     __syncthreads();
 
     // (2) exclusive scan across warps per expert; tile count per expert
-    for (int e = tid; e < a.E; e += kLayoutThreads) {
+    for (int e = tid; e < a.E; e += kThreads) {
         int run = 0;
-#pragma unroll
-        for (int w = 0; w < kLayoutWarps; ++w) {
+#pragma unroll 8
+        for (int w = 0; w < W; ++w) {
             const int v = hw[w * a.E + e];
             hw[w * a.E + e] = run;
             run += v;
         }
         col_agg[e] = run;
     }
-    // (3) ranks and nodes touched by each token: a token counts once per rank / node
+
+    // (3) one thread per token: the ranks and nodes it reaches (a token counts once
+    // per rank and once per node) and its is_token_in_rank row
     const bool small_r = a.R <= 64, small_n = a.N <= 64;
-    for (int tl = tid; tl < ntok; tl += kLayoutThreads) {
-        const int *pr = pair_rk + tl * a.k;
+    for (int tl = tid; tl < ntok; tl += kThreads) {
+        const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
         unsigned long long rm = 0, nm = 0;
         for (int j = 0; j < a.k; ++j) {
-            const int r = pr[j];
-            if (r < 0) continue;
+            const int64_t v = __ldg(row + j);
+            if (v < 0 || v >= a.E) continue;
+            const int r = (int)v / a.epr;
             const int n = r / a.rpn;
             bool new_r = true, new_n = true;
             if (small_r) {
                 new_r = !((rm >> r) & 1ull);
                 rm |= 1ull << r;
             } else {
-                for (int j2 = 0; j2 < j && new_r; ++j2) new_r = pr[j2] != r;
+                for (int j2 = 0; j2 < j && new_r; ++j2) {
+                    const int64_t v2 = __ldg(row + j2);
+                    new_r = !(v2 >= 0 && v2 < a.E && (int)v2 / a.epr == r);
+                }
             }
             if (small_n) {
                 new_n = !((nm >> n) & 1ull);
                 nm |= 1ull << n;
             } else {
-                for (int j2 = 0; j2 < j && new_n; ++j2) new_n = !(pr[j2] >= 0 && pr[j2] / a.rpn == n);
+                for (int j2 = 0; j2 < j && new_n; ++j2) {
+                    const int64_t v2 = __ldg(row + j2);
+                    new_n = !(v2 >= 0 && v2 < a.E && ((int)v2 / a.epr) / a.rpn == n);
+                }
             }
             if (new_r) atomicAdd(&col_agg[a.E + r], 1);
             if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
         }
-        tok_rmask[tl] = rm;
+        if (a.in_rank) {
+            uint8_t *dst = a.in_rank + (int64_t)(t0 + tl) * a.R;
+            for (int r = 0; r < a.R; ++r) {
+                bool hit;
+                if (small_r) {
+                    hit = (rm >> r) & 1ull;
+                } else {
+                    hit = false;
+                    for (int j = 0; j < a.k && !hit; ++j) {
+                        const int64_t v = __ldg(row + j);
+                        hit = v >= 0 && v < a.E && (int)v / a.epr == r;
+                    }
+                }
+                dst[r] = hit ? 1 : 0;
+            }
+        }
     }
     __syncthreads();
 
@@ -165,27 +190,14 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     const bool publish = (tile != a.stalled_tile);
     int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
     int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
-    for (int c = tid; c < a.cols; c += kLayoutThreads) {
+    for (int c = tid; c < a.cols; c += kThreads) {
         if (tile == 0) my_incl[c] = col_agg[c];
         else my_agg[c] = col_agg[c];
     }
-    __threadfence();
     __syncthreads();
-    if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
-
-    // is_token_in_rank rows of this tile (nothing waits on them)
-    if (a.in_rank) {
-        uint8_t *rows = a.in_rank + (int64_t)t0 * a.R;
-        for (int i = tid; i < ntok * a.R; i += kLayoutThreads) {
-            const int tl = i / a.R, r = i - tl * a.R;
-            bool hit = false;
-            if (small_r) {
-                hit = (tok_rmask[tl] >> r) & 1ull;
-            } else {
-                for (int j = 0; j < a.k; ++j) hit |= pair_rk[tl * a.k + j] == r;
-            }
-            rows[i] = hit ? 1 : 0;
-        }
+    if (tid == 0 && publish) {
+        __threadfence();
+        st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
     }
 
     // (5) decoupled look-back over earlier tiles
@@ -228,7 +240,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
                         break;
                     }
                     __nanosleep(ns);
-                    if (ns < 1024) ns <<= 1;
+                    if (ns < 256) ns <<= 1;
                 }
                 if (lane == 0) {
                     s_win_aggs = win_aggs;
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
             }
             __syncthreads();
             const int wa = s_win_aggs, wi = s_win_incl, wdone = s_win_done;
-            for (int c = tid; c < a.cols; c += kLayoutThreads) {
+            for (int c = tid; c < a.cols; c += kThreads) {
                 // all window rows are loaded at once: one L2 round trip, not one per row
                 const int32_t *col = a.agg + (size_t)pos * a.cols_pad + c;
                 int sum = 0;
@@ -253,23 +265,29 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
             pos -= 32;
         }
         // (6) publish the inclusive prefix
-        for (int c = tid; c < a.cols; c += kLayoutThreads) my_incl[c] = col_excl[c] + col_agg[c];
-        __threadfence();
+        for (int c = tid; c < a.cols; c += kThreads) my_incl[c] = col_excl[c] + col_agg[c];
         __syncthreads();
-        if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | kStateIncl);
+        if (tid == 0 && publish) {
+            __threadfence();
+            st_release_gpu(&a.state[tile], tag | kStateIncl);
+        }
     }
 
     // (7) rank of every pair inside its expert over the whole batch
-    for (int p = tid; p < npairs; p += kLayoutThreads) {
-        const int e = pair_e[p];
-        const int w = (p >> 5) / cpw;
-        a.pair_rank[pair0 + p] = e >= 0 ? col_excl[e] + hw[w * a.E + e] + pair_r[p] : -1;
+    const int *my_base = hw + warp * a.E;
+#pragma unroll
+    for (int c = 0; c < kLayoutChunks; ++c) {
+        const int p = p_base + 32 * c;
+        if (p < npairs) {
+            const int e = pe[c];
+            a.pair_rank[pair0 + p] = e >= 0 ? col_excl[e] + my_base[e] + pr[c] : -1;
+        }
     }
 
     // (8) the last tile in ticket order holds the totals
     if (tile == a.tiles - 1) {
         int part = 0;
-        for (int c = tid; c < a.cols; c += kLayoutThreads) {
+        for (int c = tid; c < a.cols; c += kThreads) {
             const int tot = col_excl[c] + col_agg[c];
             if (c < a.E) {
                 a.per_expert[c] = tot;
@@ -285,7 +303,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
         __syncthreads();
         if (tid == 0) {
             int P = 0;
-            for (int w = 0; w < kLayoutWarps; ++w) P += s_red[w];
+            for (int w = 0; w < W; ++w) P += s_red[w];
             a.hdr->total_pairs = P;
             a.hdr->num_tokens = a.T;
             a.hdr->num_topk = a.k;
@@ -293,9 +311,9 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     }
 
     // (9) the last block to finish resets the call state for the next call
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
+        __threadfence();
         const unsigned prev = atomicAdd(&a.hdr->done, 1u);
         if (prev == (unsigned)a.tiles - 1) {
             a.hdr->done = 0;
@@ -306,10 +324,29 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
     }
 }
 
-size_t layout_smem_bytes(int k, int E, int cols_pad) {
-    const int tile = layout_tile_tokens(k);
-    return (size_t)tile * sizeof(unsigned long long) +
-           ((size_t)kLayoutWarps * E + 2 * (size_t)cols_pad + 3 * (size_t)tile * k) * sizeof(int);
+size_t layout_smem_bytes(int E, int cols_pad) {
+    return ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad) * sizeof(int);
+}
+
+template <int W>
+epd_status_t launch_layout(const LayoutArgs &a, size_t smem, cudaStream_t stream) {
+    auto kernel = layout_kernel<W>;
+    if (smem > 48 * 1024) {
+        // the opt-in limit covers static and dynamic shared memory together
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
+            return record_cuda_error();
+        if (smem + fa.sharedSizeBytes > (size_t)optin) return EPD_ERR_UNSUPPORTED;
+        if ((int)smem > fa.maxDynamicSharedSizeBytes &&
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+            return record_cuda_error();
+    }
+    return launch_pdl(kernel, a.tiles, W * 32, smem, stream, a);
 }
 
 epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, int N,
@@ -326,23 +363,7 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     if (spin_limit == 0) return EPD_ERR_INVALID_ARG;
 
     const WsLayout w = ws_layout(T, k, E, R, N);
-    const size_t smem = layout_smem_bytes(k, E, w.cols_pad);
-    if (smem > 48 * 1024) {
-        // the opt-in limit covers static and dynamic shared memory together
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-                cudaSuccess ||
-            cudaFuncGetAttributes(&fa, layout_kernel) != cudaSuccess)
-            return record_cuda_error();
-        if (smem + fa.sharedSizeBytes > (size_t)optin) return EPD_ERR_UNSUPPORTED;
-        if ((int)smem > fa.maxDynamicSharedSizeBytes &&
-            cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return record_cuda_error();
-    }
-
+    const size_t smem = layout_smem_bytes(E, w.cols_pad);
     char *ws = static_cast<char *>(workspace);
     LayoutArgs a;
     a.topk = topk_idx;
@@ -363,13 +384,18 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.agg = reinterpret_cast<int32_t *>(ws + w.agg_off);
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
     a.tiles = w.tiles;
-    a.tile_tokens = layout_tile_tokens(k);
+    a.tile_tokens = layout_tile_tokens(k, E);
     a.cols = w.cols;
     a.cols_pad = w.cols_pad;
     a.status = status;
     a.stalled_tile = stalled_tile;
     a.spin_limit = spin_limit;
-    return launch_pdl(layout_kernel, w.tiles, kLayoutThreads, smem, stream, a);
+    switch (layout_warps(E)) {
+        case 32: return launch_layout<32>(a, smem, stream);
+        case 16: return launch_layout<16>(a, smem, stream);
+        case 8: return launch_layout<8>(a, smem, stream);
+        default: return launch_layout<4>(a, smem, stream);
+    }
 }
 
 }  // namespace
