@@ -39,10 +39,14 @@ __host__ __device__ inline int layout_warps(int E) {
     return E <= 512 ? 32 : E <= 1024 ? 16 : E <= 2048 ? 8 : 4;
 }
 
-// Tokens per layout tile: the tile holds at most 256 (token, pick) pairs per warp.
+constexpr int kLayoutMaxTileTokens = 2048;
+
+// Tokens per layout tile: at most 256 (token, pick) pairs per warp and at most
+// 2048 tokens (one 64-bit rank mask per token stays in shared memory).
 __host__ __device__ inline int layout_tile_tokens(int k, int E) {
     const int pairs = kLayoutPairsPerWarp * layout_warps(E);
-    return k > 0 ? pairs / k : pairs;
+    const int t = k > 0 ? pairs / k : pairs;
+    return t < kLayoutMaxTileTokens ? t : kLayoutMaxTileTokens;
 }
 
 struct WsLayout {

@@ -61,7 +61,8 @@ template <int W>
 __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
     extern __shared__ int4 smem_raw[];
-    int *hw = reinterpret_cast<int *>(smem_raw);  // [W][E] warp histograms -> warp bases
+    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);
+    int *hw = reinterpret_cast<int *>(tok_rmask + kLayoutMaxTileTokens);  // [W][E] -> warp bases
     int *col_agg = hw + W * a.E;                   // [cols_pad] this tile's counts
     int *col_excl = col_agg + a.cols_pad;          // [cols_pad] counts of earlier tiles
     __shared__ int s_tile;
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     }
 
     // (3) one thread per token: the ranks and nodes it reaches (a token counts once
-    // per rank and once per node) and its is_token_in_rank row
+    // per rank and once per node); with R <= 64 its ranks are kept as a bit mask
     const bool small_r = a.R <= 64, small_n = a.N <= 64;
     for (int tl = tid; tl < ntok; tl += kThreads) {
         const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
@@ -167,24 +168,37 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
             if (new_r) atomicAdd(&col_agg[a.E + r], 1);
             if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
         }
-        if (a.in_rank) {
-            uint8_t *dst = a.in_rank + (int64_t)(t0 + tl) * a.R;
-            for (int r = 0; r < a.R; ++r) {
-                bool hit;
-                if (small_r) {
-                    hit = (rm >> r) & 1ull;
-                } else {
-                    hit = false;
-                    for (int j = 0; j < a.k && !hit; ++j) {
-                        const int64_t v = __ldg(row + j);
-                        hit = v >= 0 && v < a.E && (int)v / a.epr == r;
-                    }
-                }
-                dst[r] = hit ? 1 : 0;
-            }
-        }
+        tok_rmask[tl] = rm;
     }
     __syncthreads();
+
+    // is_token_in_rank rows of the tile: one contiguous [ntok, R] byte block,
+    // written in coalesced 4-byte words where the block is 4-byte aligned
+    if (a.in_rank) {
+        uint8_t *blk = a.in_rank + (int64_t)t0 * a.R;
+        const int nbytes = ntok * a.R;
+        auto byte_at = [&](int i) -> uint32_t {
+            const int tl = i / a.R, r = i - tl * a.R;
+            if (small_r) return (uint32_t)((tok_rmask[tl] >> r) & 1ull);
+            const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+            for (int j = 0; j < a.k; ++j) {
+                const int64_t v = __ldg(row + j);
+                if (v >= 0 && v < a.E && (int)v / a.epr == r) return 1u;
+            }
+            return 0u;
+        };
+        const int head = (int)((4 - (reinterpret_cast<uintptr_t>(blk) & 3)) & 3);
+        const int lead = min(head, nbytes);
+        for (int i = tid; i < lead; i += kThreads) blk[i] = (uint8_t)byte_at(i);
+        const int nwords = (nbytes - lead) >> 2;
+        uint32_t *words = reinterpret_cast<uint32_t *>(blk + lead);
+        for (int wi = tid; wi < nwords; wi += kThreads) {
+            const int i = lead + 4 * wi;
+            words[wi] = byte_at(i) | (byte_at(i + 1) << 8) | (byte_at(i + 2) << 16) |
+                        (byte_at(i + 3) << 24);
+        }
+        for (int i = lead + 4 * nwords + tid; i < nbytes; i += kThreads) blk[i] = (uint8_t)byte_at(i);
+    }
 
     // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its prefix)
     const bool publish = (tile != a.stalled_tile);
@@ -325,7 +339,8 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
 }
 
 size_t layout_smem_bytes(int E, int cols_pad) {
-    return ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad) * sizeof(int);
+    return (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
+           ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad) * sizeof(int);
 }
 
 template <int W>
