@@ -135,40 +135,56 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         col_agg[e] = run;
     }
 
-    // (3) one thread per token: the ranks and nodes it reaches (a token counts once
-    // per rank and once per node); with R <= 64 its ranks are kept as a bit mask
+    // (3) one lane per token: the ranks and nodes it reaches (a token counts once
+    // per rank and once per node). With R, N <= 64 each token's ranks and nodes
+    // are bit masks and a warp adds its 32 tokens' counts with one ballot and one
+    // shared-memory add per rank / node, instead of one add per token.
     const bool small_r = a.R <= 64, small_n = a.N <= 64;
-    for (int tl = tid; tl < ntok; tl += kThreads) {
-        const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+    for (int base = warp * 32; base < ntok; base += kThreads) {
+        const int tl = base + lane;
         unsigned long long rm = 0, nm = 0;
-        for (int j = 0; j < a.k; ++j) {
-            const int64_t v = __ldg(row + j);
-            if (v < 0 || v >= a.E) continue;
-            const int r = (int)v / a.epr;
-            const int n = r / a.rpn;
-            bool new_r = true, new_n = true;
-            if (small_r) {
-                new_r = !((rm >> r) & 1ull);
-                rm |= 1ull << r;
-            } else {
-                for (int j2 = 0; j2 < j && new_r; ++j2) {
-                    const int64_t v2 = __ldg(row + j2);
-                    new_r = !(v2 >= 0 && v2 < a.E && (int)v2 / a.epr == r);
+        if (tl < ntok) {
+            const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+            for (int j = 0; j < a.k; ++j) {
+                const int64_t v = __ldg(row + j);
+                if (v < 0 || v >= a.E) continue;
+                const int r = (int)v / a.epr;
+                const int n = r / a.rpn;
+                if (small_r) {
+                    rm |= 1ull << r;
+                } else {
+                    bool new_r = true;
+                    for (int j2 = 0; j2 < j && new_r; ++j2) {
+                        const int64_t v2 = __ldg(row + j2);
+                        new_r = !(v2 >= 0 && v2 < a.E && (int)v2 / a.epr == r);
+                    }
+                    if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+                }
+                if (small_n) {
+                    nm |= 1ull << n;
+                } else {
+                    bool new_n = true;
+                    for (int j2 = 0; j2 < j && new_n; ++j2) {
+                        const int64_t v2 = __ldg(row + j2);
+                        new_n = !(v2 >= 0 && v2 < a.E && ((int)v2 / a.epr) / a.rpn == n);
+                    }
+                    if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                 }
             }
-            if (small_n) {
-                new_n = !((nm >> n) & 1ull);
-                nm |= 1ull << n;
-            } else {
-                for (int j2 = 0; j2 < j && new_n; ++j2) {
-                    const int64_t v2 = __ldg(row + j2);
-                    new_n = !(v2 >= 0 && v2 < a.E && ((int)v2 / a.epr) / a.rpn == n);
-                }
-            }
-            if (new_r) atomicAdd(&col_agg[a.E + r], 1);
-            if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
+            tok_rmask[tl] = rm;
         }
-        tok_rmask[tl] = rm;
+        if (small_r) {
+            for (int r = 0; r < a.R; ++r) {
+                const uint32_t b = __ballot_sync(0xffffffffu, (rm >> r) & 1ull);
+                if (lane == 0 && b) atomicAdd(&col_agg[a.E + r], __popc(b));
+            }
+        }
+        if (small_n) {
+            for (int n = 0; n < a.N; ++n) {
+                const uint32_t b = __ballot_sync(0xffffffffu, (nm >> n) & 1ull);
+                if (lane == 0 && b) atomicAdd(&col_agg[a.E + a.R + n], __popc(b));
+            }
+        }
     }
     __syncthreads();
 
