@@ -34,10 +34,8 @@ constexpr int kLayoutPairsPerWarp = 32 * kLayoutChunks;
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Warps per layout block: each warp keeps a private E-wide histogram in shared
-// memory, so fewer warps for larger E (at most 64 KiB of histograms).
-__host__ __device__ inline int layout_warps(int E) {
-    return E <= 512 ? 32 : E <= 1024 ? 16 : E <= 2048 ? 8 : 4;
-}
+// memory (at most 64 KiB of histograms).
+__host__ __device__ inline int layout_warps(int E) { return E <= 2048 ? 8 : 4; }
 
 constexpr int kLayoutMaxTileTokens = 2048;
 

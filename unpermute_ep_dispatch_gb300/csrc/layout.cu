@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     int *hw = reinterpret_cast<int *>(tok_rmask + kLayoutMaxTileTokens);  // [W][E] -> warp bases
     int *col_agg = hw + W * a.E;                   // [cols_pad] this tile's counts
     int *col_excl = col_agg + a.cols_pad;          // [cols_pad] counts of earlier tiles
+    int *rank_of = col_excl + a.cols_pad;          // [E] simulated rank of each expert
+    int *node_of = rank_of + a.E;                  // [R] simulated node of each rank
     __shared__ int s_tile;
     __shared__ uint32_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         col_agg[i] = 0;
         col_excl[i] = 0;
     }
+    for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
+    for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
     pdl_wait();  // the workspace and topk_idx may come from the previous kernel
     pdl_trigger();
     if (tid == 0) {
@@ -148,15 +152,15 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
             for (int j = 0; j < a.k; ++j) {
                 const int64_t v = __ldg(row + j);
                 if (v < 0 || v >= a.E) continue;
-                const int r = (int)v / a.epr;
-                const int n = r / a.rpn;
+                const int r = rank_of[v];
+                const int n = node_of[r];
                 if (small_r) {
                     rm |= 1ull << r;
                 } else {
                     bool new_r = true;
                     for (int j2 = 0; j2 < j && new_r; ++j2) {
                         const int64_t v2 = __ldg(row + j2);
-                        new_r = !(v2 >= 0 && v2 < a.E && (int)v2 / a.epr == r);
+                        new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
                     }
                     if (new_r) atomicAdd(&col_agg[a.E + r], 1);
                 }
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
                     bool new_n = true;
                     for (int j2 = 0; j2 < j && new_n; ++j2) {
                         const int64_t v2 = __ldg(row + j2);
-                        new_n = !(v2 >= 0 && v2 < a.E && ((int)v2 / a.epr) / a.rpn == n);
+                        new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
                     }
                     if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                 }
@@ -189,31 +193,35 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     __syncthreads();
 
     // is_token_in_rank rows of the tile: one contiguous [ntok, R] byte block,
-    // written in coalesced 4-byte words where the block is 4-byte aligned
+    // written in coalesced 4-byte words where it is 4-byte aligned
     if (a.in_rank) {
         uint8_t *blk = a.in_rank + (int64_t)t0 * a.R;
         const int nbytes = ntok * a.R;
-        auto byte_at = [&](int i) -> uint32_t {
-            const int tl = i / a.R, r = i - tl * a.R;
-            if (small_r) return (uint32_t)((tok_rmask[tl] >> r) & 1ull);
-            const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
-            for (int j = 0; j < a.k; ++j) {
-                const int64_t v = __ldg(row + j);
-                if (v >= 0 && v < a.E && (int)v / a.epr == r) return 1u;
+        if (small_r && (a.R & 3) == 0 && (reinterpret_cast<uintptr_t>(blk) & 3) == 0) {
+            // each word holds 4 ranks of one token: spread 4 mask bits into 4 bytes
+            const int wpr = a.R >> 2;  // words per row
+            uint32_t *words = reinterpret_cast<uint32_t *>(blk);
+            for (int wi = tid; wi < (nbytes >> 2); wi += kThreads) {
+                const int tl = wi / wpr;
+                const uint32_t m = (uint32_t)(tok_rmask[tl] >> ((wi - tl * wpr) << 2)) & 0xFu;
+                words[wi] = (m & 1u) | ((m & 2u) << 7) | ((m & 4u) << 14) | ((m & 8u) << 21);
             }
-            return 0u;
-        };
-        const int head = (int)((4 - (reinterpret_cast<uintptr_t>(blk) & 3)) & 3);
-        const int lead = min(head, nbytes);
-        for (int i = tid; i < lead; i += kThreads) blk[i] = (uint8_t)byte_at(i);
-        const int nwords = (nbytes - lead) >> 2;
-        uint32_t *words = reinterpret_cast<uint32_t *>(blk + lead);
-        for (int wi = tid; wi < nwords; wi += kThreads) {
-            const int i = lead + 4 * wi;
-            words[wi] = byte_at(i) | (byte_at(i + 1) << 8) | (byte_at(i + 2) << 16) |
-                        (byte_at(i + 3) << 24);
+        } else {
+            for (int i = tid; i < nbytes; i += kThreads) {
+                const int tl = i / a.R, r = i - tl * a.R;
+                bool hit = false;
+                if (small_r) {
+                    hit = (tok_rmask[tl] >> r) & 1ull;
+                } else {
+                    const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+                    for (int j = 0; j < a.k && !hit; ++j) {
+                        const int64_t v = __ldg(row + j);
+                        hit = v >= 0 && v < a.E && rank_of[v] == r;
+                    }
+                }
+                blk[i] = hit ? 1 : 0;
+            }
         }
-        for (int i = lead + 4 * nwords + tid; i < nbytes; i += kThreads) blk[i] = (uint8_t)byte_at(i);
     }
 
     // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its prefix)
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
 
 size_t layout_smem_bytes(int E, int cols_pad) {
     return (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
-           ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad) * sizeof(int);
+           ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int);
 }
 
 template <int W>
@@ -421,12 +429,8 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.status = status;
     a.stalled_tile = stalled_tile;
     a.spin_limit = spin_limit;
-    switch (layout_warps(E)) {
-        case 32: return launch_layout<32>(a, smem, stream);
-        case 16: return launch_layout<16>(a, smem, stream);
-        case 8: return launch_layout<8>(a, smem, stream);
-        default: return launch_layout<4>(a, smem, stream);
-    }
+    if (layout_warps(E) == 8) return launch_layout<8>(a, smem, stream);
+    return launch_layout<4>(a, smem, stream);
 }
 
 }  // namespace
