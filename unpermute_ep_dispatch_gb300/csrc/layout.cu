@@ -46,6 +46,7 @@ struct LayoutArgs {
     uint32_t *state;
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
+    int id_bits;  // bits needed for an expert id in [0, E)
     int32_t *status;
     int stalled_tile;
     uint32_t spin_limit;
@@ -97,8 +98,9 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
 
     // (1) warp w owns pairs [256 w, 256 w + 256) of the tile, in row-major order.
     // All of a lane's picks are loaded at once, then each 32-pair chunk is ranked:
-    // lanes holding the same expert find each other with __match_any_sync and the
-    // lowest of them adds the group's size to the warp's private histogram.
+    // lanes holding the same expert find each other with one ballot per bit of the
+    // expert id, and the lowest of them adds the group's size to the warp's
+    // private histogram.
     int pe[kLayoutChunks], pr[kLayoutChunks];
     const int p_base = warp * kLayoutPairsPerWarp + lane;
 #pragma unroll
@@ -115,8 +117,12 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         const int e = pe[c];
         const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
         pr[c] = 0;
+        uint32_t peers = valid;
+        for (int b = 0; b < a.id_bits; ++b) {
+            const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
+            peers &= ((e >> b) & 1) ? set : ~set;
+        }
         if (e >= 0) {
-            const uint32_t peers = __match_any_sync(valid, e);
             const int before = __popc(peers & lanemask_lt());
             const int base = my_hist[e];
             pr[c] = base + before;
@@ -149,30 +155,37 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         unsigned long long rm = 0, nm = 0;
         if (tl < ntok) {
             const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
-            for (int j = 0; j < a.k; ++j) {
-                const int64_t v = __ldg(row + j);
-                if (v < 0 || v >= a.E) continue;
-                const int r = rank_of[v];
-                const int n = node_of[r];
-                if (small_r) {
-                    rm |= 1ull << r;
-                } else {
-                    bool new_r = true;
-                    for (int j2 = 0; j2 < j && new_r; ++j2) {
-                        const int64_t v2 = __ldg(row + j2);
-                        new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
+            for (int j0 = 0; j0 < a.k; j0 += 8) {
+                int64_t vv[8];  // one batch of loads for up to 8 picks
+#pragma unroll
+                for (int q = 0; q < 8; ++q) vv[q] = (j0 + q < a.k) ? __ldg(row + j0 + q) : -1;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = j0 + q;
+                    const int64_t v = vv[q];
+                    if (v < 0 || v >= a.E) continue;
+                    const int r = rank_of[v];
+                    const int n = node_of[r];
+                    if (small_r) {
+                        rm |= 1ull << r;
+                    } else {
+                        bool new_r = true;
+                        for (int j2 = 0; j2 < j && new_r; ++j2) {
+                            const int64_t v2 = __ldg(row + j2);
+                            new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
+                        }
+                        if (new_r) atomicAdd(&col_agg[a.E + r], 1);
                     }
-                    if (new_r) atomicAdd(&col_agg[a.E + r], 1);
-                }
-                if (small_n) {
-                    nm |= 1ull << n;
-                } else {
-                    bool new_n = true;
-                    for (int j2 = 0; j2 < j && new_n; ++j2) {
-                        const int64_t v2 = __ldg(row + j2);
-                        new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
+                    if (small_n) {
+                        nm |= 1ull << n;
+                    } else {
+                        bool new_n = true;
+                        for (int j2 = 0; j2 < j && new_n; ++j2) {
+                            const int64_t v2 = __ldg(row + j2);
+                            new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
+                        }
+                        if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                     }
-                    if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                 }
             }
             tok_rmask[tl] = rm;
@@ -192,8 +205,23 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     }
     __syncthreads();
 
-    // is_token_in_rank rows of the tile: one contiguous [ntok, R] byte block,
-    // written in coalesced 4-byte words where it is 4-byte aligned
+    // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its prefix)
+    const bool publish = (tile != a.stalled_tile);
+    int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
+    int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
+    for (int c = tid; c < a.cols; c += kThreads) {
+        if (tile == 0) my_incl[c] = col_agg[c];
+        else my_agg[c] = col_agg[c];
+    }
+    __syncthreads();
+    if (tid == 0 && publish) {
+        __threadfence();
+        st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
+    }
+
+    // is_token_in_rank rows of the tile, after publishing (nothing waits on them):
+    // one contiguous [ntok, R] byte block, written in coalesced 4-byte words where
+    // it is 4-byte aligned
     if (a.in_rank) {
         uint8_t *blk = a.in_rank + (int64_t)t0 * a.R;
         const int nbytes = ntok * a.R;
@@ -222,20 +250,6 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
                 blk[i] = hit ? 1 : 0;
             }
         }
-    }
-
-    // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its prefix)
-    const bool publish = (tile != a.stalled_tile);
-    int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
-    int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
-    for (int c = tid; c < a.cols; c += kThreads) {
-        if (tile == 0) my_incl[c] = col_agg[c];
-        else my_agg[c] = col_agg[c];
-    }
-    __syncthreads();
-    if (tid == 0 && publish) {
-        __threadfence();
-        st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
     }
 
     // (5) decoupled look-back over earlier tiles
@@ -424,6 +438,8 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
     a.tiles = w.tiles;
     a.tile_tokens = layout_tile_tokens(k, E);
+    a.id_bits = 0;
+    while ((1 << a.id_bits) < E) ++a.id_bits;
     a.cols = w.cols;
     a.cols_pad = w.cols_pad;
     a.status = status;
