@@ -28,23 +28,22 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 64, "header is one 64-byte block");
 
 constexpr size_t kAlign = 256;
-constexpr int kLayoutChunks = 8;                       // 32-pair chunks per layout warp
-constexpr int kLayoutPairsPerWarp = 32 * kLayoutChunks;
+constexpr int kLayoutTilePairs = 2048;     // (token, pick) pairs per layout tile
+constexpr int kLayoutMaxTileTokens = 2048;
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Warps per layout block: each warp keeps a private E-wide histogram in shared
-// memory (at most 64 KiB of histograms).
-__host__ __device__ inline int layout_warps(int E) { return E <= 2048 ? 8 : 4; }
+// memory (at most 64 KiB of histograms), so fewer warps for larger E.
+__host__ __device__ inline int layout_warps(int E) {
+    return E <= 512 ? 32 : E <= 1024 ? 16 : E <= 2048 ? 8 : 4;
+}
 
-constexpr int kLayoutMaxTileTokens = 2048;
-
-// Tokens per layout tile: at most 256 (token, pick) pairs per warp and at most
-// 2048 tokens (one 64-bit rank mask per token stays in shared memory).
-__host__ __device__ inline int layout_tile_tokens(int k, int E) {
-    const int pairs = kLayoutPairsPerWarp * layout_warps(E);
-    const int t = k > 0 ? pairs / k : pairs;
-    return t < kLayoutMaxTileTokens ? t : kLayoutMaxTileTokens;
+// Tokens per layout tile: at most 2048 pairs and at most 2048 tokens (one 64-bit
+// rank mask and one node mask per token stay in shared memory).
+__host__ __device__ inline int layout_tile_tokens(int k) {
+    const int t = k > 0 ? kLayoutTilePairs / k : kLayoutMaxTileTokens;
+    return t < 1 ? 1 : (t < kLayoutMaxTileTokens ? t : kLayoutMaxTileTokens);
 }
 
 struct WsLayout {
@@ -56,7 +55,7 @@ __host__ __device__ inline size_t ws_pair_rank_off() { return kAlign; }
 
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N) {
     WsLayout w;
-    int tile = layout_tile_tokens(k, E);
+    int tile = layout_tile_tokens(k);
     w.tiles = T > 0 ? (T + tile - 1) / tile : 1;
     w.cols = E + R + N;
     w.cols_pad = (int)align_up((size_t)w.cols, 32);

@@ -61,13 +61,15 @@ __device__ __forceinline__ int warp_sum(int v) {
 template <int W>
 __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
+    constexpr int kChunks = kLayoutTilePairs / kThreads;  // 32-pair chunks per warp
     extern __shared__ int4 smem_raw[];
-    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);
-    int *hw = reinterpret_cast<int *>(tok_rmask + kLayoutMaxTileTokens);  // [W][E] -> warp bases
-    int *col_agg = hw + W * a.E;                   // [cols_pad] this tile's counts
-    int *col_excl = col_agg + a.cols_pad;          // [cols_pad] counts of earlier tiles
-    int *rank_of = col_excl + a.cols_pad;          // [E] simulated rank of each expert
-    int *node_of = rank_of + a.E;                  // [R] simulated node of each rank
+    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);  // ranks
+    unsigned long long *tok_nmask = tok_rmask + kLayoutMaxTileTokens;                 // nodes
+    int *hw = reinterpret_cast<int *>(tok_nmask + kLayoutMaxTileTokens);  // [W][E] -> warp bases
+    int *col_agg = hw + W * a.E;           // [cols_pad] this tile's counts
+    int *col_excl = col_agg + a.cols_pad;  // [cols_pad] counts of earlier tiles
+    int *rank_of = col_excl + a.cols_pad;  // [E] simulated rank of each expert
+    int *node_of = rank_of + a.E;          // [R] simulated node of each rank
     __shared__ int s_tile;
     __shared__ uint32_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
@@ -96,15 +98,15 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     const int npairs = ntok * a.k;
     const int64_t pair0 = (int64_t)t0 * a.k;
 
-    // (1) warp w owns pairs [256 w, 256 w + 256) of the tile, in row-major order.
-    // All of a lane's picks are loaded at once, then each 32-pair chunk is ranked:
-    // lanes holding the same expert find each other with one ballot per bit of the
-    // expert id, and the lowest of them adds the group's size to the warp's
-    // private histogram.
-    int pe[kLayoutChunks], pr[kLayoutChunks];
-    const int p_base = warp * kLayoutPairsPerWarp + lane;
+    // (1) warp w owns a contiguous run of kChunks 32-pair chunks of the tile, in
+    // row-major order. All of a lane's picks are loaded at once, then each chunk
+    // is ranked: lanes holding the same expert find each other with one ballot per
+    // bit of the expert id, and the lowest of them adds the group's size to the
+    // warp's private histogram.
+    int pe[kChunks], pr[kChunks];
+    const int p_base = warp * 32 * kChunks + lane;
 #pragma unroll
-    for (int c = 0; c < kLayoutChunks; ++c) {
+    for (int c = 0; c < kChunks; ++c) {
         const int p = p_base + 32 * c;
         int64_t v = -1;
         if (p < npairs) v = __ldg(a.topk + pair0 + p);
@@ -113,15 +115,14 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     }
     int *my_hist = hw + warp * a.E;
 #pragma unroll
-    for (int c = 0; c < kLayoutChunks; ++c) {
+    for (int c = 0; c < kChunks; ++c) {
         const int e = pe[c];
-        const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
-        pr[c] = 0;
-        uint32_t peers = valid;
+        uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
         for (int b = 0; b < a.id_bits; ++b) {
             const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
             peers &= ((e >> b) & 1) ? set : ~set;
         }
+        pr[c] = 0;
         if (e >= 0) {
             const int before = __popc(peers & lanemask_lt());
             const int base = my_hist[e];
@@ -131,81 +132,83 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         }
         __syncwarp();
     }
-    __syncthreads();
 
-    // (2) exclusive scan across warps per expert; tile count per expert
-    for (int e = tid; e < a.E; e += kThreads) {
-        int run = 0;
-#pragma unroll 8
-        for (int w = 0; w < W; ++w) {
-            const int v = hw[w * a.E + e];
-            hw[w * a.E + e] = run;
-            run += v;
-        }
-        col_agg[e] = run;
-    }
-
-    // (3) one lane per token: the ranks and nodes it reaches (a token counts once
-    // per rank and once per node). With R, N <= 64 each token's ranks and nodes
-    // are bit masks and a warp adds its 32 tokens' counts with one ballot and one
-    // shared-memory add per rank / node, instead of one add per token.
+    // (3a) one thread per token: the ranks and nodes it reaches, as bit masks when
+    // R, N <= 64 (a token counts once per rank and once per node)
     const bool small_r = a.R <= 64, small_n = a.N <= 64;
-    for (int base = warp * 32; base < ntok; base += kThreads) {
-        const int tl = base + lane;
+    for (int tl = tid; tl < ntok; tl += kThreads) {
+        const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
         unsigned long long rm = 0, nm = 0;
-        if (tl < ntok) {
-            const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
-            for (int j0 = 0; j0 < a.k; j0 += 8) {
-                int64_t vv[8];  // one batch of loads for up to 8 picks
+        for (int j0 = 0; j0 < a.k; j0 += 8) {
+            int64_t vv[8];  // one batch of loads for up to 8 picks
 #pragma unroll
-                for (int q = 0; q < 8; ++q) vv[q] = (j0 + q < a.k) ? __ldg(row + j0 + q) : -1;
+            for (int q = 0; q < 8; ++q) vv[q] = (j0 + q < a.k) ? __ldg(row + j0 + q) : -1;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = j0 + q;
-                    const int64_t v = vv[q];
-                    if (v < 0 || v >= a.E) continue;
-                    const int r = rank_of[v];
-                    const int n = node_of[r];
-                    if (small_r) {
-                        rm |= 1ull << r;
-                    } else {
-                        bool new_r = true;
-                        for (int j2 = 0; j2 < j && new_r; ++j2) {
-                            const int64_t v2 = __ldg(row + j2);
-                            new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
-                        }
-                        if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+            for (int q = 0; q < 8; ++q) {
+                const int j = j0 + q;
+                const int64_t v = vv[q];
+                if (v < 0 || v >= a.E) continue;
+                const int r = rank_of[v];
+                const int n = node_of[r];
+                if (small_r) {
+                    rm |= 1ull << r;
+                } else {
+                    bool new_r = true;
+                    for (int j2 = 0; j2 < j && new_r; ++j2) {
+                        const int64_t v2 = __ldg(row + j2);
+                        new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
                     }
-                    if (small_n) {
-                        nm |= 1ull << n;
-                    } else {
-                        bool new_n = true;
-                        for (int j2 = 0; j2 < j && new_n; ++j2) {
-                            const int64_t v2 = __ldg(row + j2);
-                            new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
-                        }
-                        if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
+                    if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+                }
+                if (small_n) {
+                    nm |= 1ull << n;
+                } else {
+                    bool new_n = true;
+                    for (int j2 = 0; j2 < j && new_n; ++j2) {
+                        const int64_t v2 = __ldg(row + j2);
+                        new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
                     }
+                    if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                 }
             }
-            tok_rmask[tl] = rm;
         }
-        if (small_r) {
-            for (int r = 0; r < a.R; ++r) {
-                const uint32_t b = __ballot_sync(0xffffffffu, (rm >> r) & 1ull);
-                if (lane == 0 && b) atomicAdd(&col_agg[a.E + r], __popc(b));
-            }
-        }
-        if (small_n) {
-            for (int n = 0; n < a.N; ++n) {
-                const uint32_t b = __ballot_sync(0xffffffffu, (nm >> n) & 1ull);
-                if (lane == 0 && b) atomicAdd(&col_agg[a.E + a.R + n], __popc(b));
-            }
-        }
+        tok_rmask[tl] = rm;
+        tok_nmask[tl] = nm;
     }
     __syncthreads();
 
-    // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its prefix)
+    // (2) exclusive scan of the warp histograms per expert (warp-shuffle scan over
+    // the W warps), and the tile's count per expert
+    for (int e = warp; e < a.E; e += W) {
+        const int v = lane < W ? hw[lane * a.E + e] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane < W) hw[lane * a.E + e] = incl - v;
+        if (lane == 31) col_agg[e] = incl;
+    }
+    // (3b) tokens per rank and per node from the masks: one thread per
+    // (rank or node, 32-token chunk)
+    const int nch = (ntok + 31) >> 5;
+    const int nr = small_r ? a.R : 0, nn = small_n ? a.N : 0;
+    for (int i = tid; i < nch * (nr + nn); i += kThreads) {
+        const int ch = i / (nr + nn), c = i - ch * (nr + nn);
+        const bool is_rank = c < nr;
+        const unsigned long long *m = is_rank ? tok_rmask : tok_nmask;
+        const int bit = is_rank ? c : c - nr;
+        int cnt = 0;
+        const int t_end = min(ntok, (ch + 1) * 32);
+        for (int t = ch * 32; t < t_end; ++t) cnt += (int)((m[t] >> bit) & 1ull);
+        if (cnt) atomicAdd(&col_agg[a.E + (is_rank ? bit : a.R + bit)], cnt);
+    }
+    __syncthreads();
+
+    // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its
+    // prefix). The block barrier orders every thread's stores before thread 0's
+    // release store of the state word.
     const bool publish = (tile != a.stalled_tile);
     int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
     int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
@@ -214,10 +217,8 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         else my_agg[c] = col_agg[c];
     }
     __syncthreads();
-    if (tid == 0 && publish) {
-        __threadfence();
+    if (tid == 0 && publish)
         st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
-    }
 
     // is_token_in_rank rows of the tile, after publishing (nothing waits on them):
     // one contiguous [ntok, R] byte block, written in coalesced 4-byte words where
@@ -316,19 +317,16 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
             if (wdone) break;
             pos -= 32;
         }
-        // (6) publish the inclusive prefix
+        // (6) publish the inclusive prefix (later tiles may be waiting on it)
         for (int c = tid; c < a.cols; c += kThreads) my_incl[c] = col_excl[c] + col_agg[c];
         __syncthreads();
-        if (tid == 0 && publish) {
-            __threadfence();
-            st_release_gpu(&a.state[tile], tag | kStateIncl);
-        }
+        if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | kStateIncl);
     }
 
     // (7) rank of every pair inside its expert over the whole batch
     const int *my_base = hw + warp * a.E;
 #pragma unroll
-    for (int c = 0; c < kLayoutChunks; ++c) {
+    for (int c = 0; c < kChunks; ++c) {
         const int p = p_base + 32 * c;
         if (p < npairs) {
             const int e = pe[c];
@@ -365,7 +363,6 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     // (9) the last block to finish resets the call state for the next call
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
         const unsigned prev = atomicAdd(&a.hdr->done, 1u);
         if (prev == (unsigned)a.tiles - 1) {
             a.hdr->done = 0;
@@ -377,7 +374,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
 }
 
 size_t layout_smem_bytes(int E, int cols_pad) {
-    return (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
+    return 2 * (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
            ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int);
 }
 
@@ -437,7 +434,7 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.agg = reinterpret_cast<int32_t *>(ws + w.agg_off);
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
     a.tiles = w.tiles;
-    a.tile_tokens = layout_tile_tokens(k, E);
+    a.tile_tokens = layout_tile_tokens(k);
     a.id_bits = 0;
     while ((1 << a.id_bits) < E) ++a.id_bits;
     a.cols = w.cols;
@@ -445,8 +442,12 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.status = status;
     a.stalled_tile = stalled_tile;
     a.spin_limit = spin_limit;
-    if (layout_warps(E) == 8) return launch_layout<8>(a, smem, stream);
-    return launch_layout<4>(a, smem, stream);
+    switch (layout_warps(E)) {
+        case 32: return launch_layout<32>(a, smem, stream);
+        case 16: return launch_layout<16>(a, smem, stream);
+        case 8: return launch_layout<8>(a, smem, stream);
+        default: return launch_layout<4>(a, smem, stream);
+    }
 }
 
 }  // namespace
