@@ -119,6 +119,15 @@ def test_ragged_hidden_bf16():
         compare(got, want)
 
 
+def test_very_wide_rows_use_the_register_permute():
+    """Rows too wide for two shared-memory stages (128 KiB bf16 rows) take the
+    register-copy permute; the result is the same."""
+    case = workloads.make_random_case(T=33, H=65536, k=2, E=8, R=4, N=2, dtype="bf16", seed=12,
+                                      routing="uniform", p_invalid=0.2, experts="random")
+    got, want, _ = run_both(case)
+    compare(got, want)
+
+
 def test_side_stream():
     s = torch.cuda.Stream()
     case = workloads.make_case("tiny")

@@ -121,6 +121,161 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
         a.m_indices[s] = -1;
 }
 
+// ----------------------------------------------------------------------------- bulk-copy variant
+// One block per SM, each over a contiguous run of tokens. For a batch of tokens
+// all threads first resolve the slots; then thread 0 streams the rows through a
+// ring of shared-memory stages -- one bulk load of each row from HBM and, as soon
+// as it lands, k bulk stores of it to its slots -- while the other warps copy the
+// small fp8 scale rows. The row copies run on the TMA engine instead of the
+// load/store units, whose store queue limits the register variant above.
+constexpr int kTmaThreads = 256;
+constexpr size_t kTmaStageBudget = 192 * 1024;  // shared memory for row stages
+constexpr int kTmaMaxStages = 16;
+constexpr uint32_t kTmaWaitLimit = 1u << 24;    // mbarrier polls before a wait gives up
+
+__host__ __device__ inline int tma_batch_tokens(int k) {
+    const int b = k > 0 ? 4096 / k : 512;
+    return b < 1 ? 1 : (b > 512 ? 512 : b);
+}
+
+struct TmaSmem {
+    int stages;
+    size_t row_stride, slots_off, list_off, bars_off, total;
+};
+
+__host__ __device__ inline TmaSmem tma_smem(int64_t row_bytes, int k) {
+    TmaSmem m;
+    m.row_stride = align_up((size_t)row_bytes, 128);
+    const size_t fit = kTmaStageBudget / m.row_stride;
+    m.stages = (int)(fit < (size_t)kTmaMaxStages ? fit : (size_t)kTmaMaxStages);
+    const int B = tma_batch_tokens(k);
+    m.slots_off = (size_t)m.stages * m.row_stride;
+    m.list_off = align_up(m.slots_off + (size_t)B * (k > 0 ? k : 1) * 4, 16);
+    m.bars_off = align_up(m.list_off + (size_t)B * 4, 16);
+    m.total = m.bars_off + (size_t)m.stages * 8;
+    return m;
+}
+
+__global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a) {
+    extern __shared__ __align__(128) uint8_t tsm[];
+    __shared__ int s_ok, s_P, s_n, s_failed;
+    const TmaSmem L = tma_smem(a.row_bytes, a.k);
+    uint8_t *stage = tsm;
+    int *s_slot = reinterpret_cast<int *>(tsm + L.slots_off);  // [batch tokens][k]
+    int *s_list = reinterpret_cast<int *>(tsm + L.list_off);   // tokens of the batch with a slot
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tsm + L.bars_off);
+    const int tid = threadIdx.x;
+    pdl_wait();  // offsets and pair ranks come from the previous kernels
+    pdl_trigger();
+    if (tid == 0) {
+        const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
+        s_ok = ok;
+        s_P = ok ? max(0, a.hdr->total_pairs) : 0;
+        s_failed = 0;
+        if (!ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
+        for (int i = 0; i < L.stages; ++i) mbar_init(&bars[i], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (!s_ok) return;
+
+    const int B = tma_batch_tokens(a.k);
+    const int S = L.stages;
+    const uint32_t bytes = (uint32_t)a.row_bytes;
+    const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
+    const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    uint32_t seq = 0;  // rows this block has loaded so far: row r uses stage r % S, phase r / S
+    for (int b0 = t_begin; b0 < t_end; b0 += B) {
+        const int nb = min(B, t_end - b0);
+        if (tid == 0) s_n = 0;
+        __syncthreads();
+        for (int i = tid; i < nb * a.k; i += kTmaThreads) {
+            const int tl = i / a.k;
+            const int64_t idx = (int64_t)(b0 + tl) * a.k + (i - tl * a.k);
+            const int64_t e = a.topk[idx];
+            int s = -1;
+            if (e >= 0 && e < a.E) {
+                const int64_t sl = (int64_t)a.start[e] + a.pair_rank[idx];
+                if (sl >= 0 && sl < a.capacity) {
+                    s = (int)sl;
+                    a.m_indices[s] = (int)e;
+                } else {
+                    report(a.status, EPD_ERR_CAPACITY);
+                }
+            }
+            a.output_index[idx] = s;
+            s_slot[i] = s;
+        }
+        __syncthreads();
+        for (int tl = tid; tl < nb; tl += kTmaThreads) {
+            bool any = false;
+            for (int j = 0; j < a.k; ++j) any |= s_slot[tl * a.k + j] >= 0;
+            if (any) s_list[atomicAdd(&s_n, 1)] = tl;  // copy order does not change the result
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const int n = s_n;
+            int issued = 0, landed = 0;
+            auto load = [&](int i) {
+                const uint32_t r = seq + i, st = r % S;
+                mbar_expect_tx(&bars[st], bytes);
+                bulk_load(stage + st * L.row_stride, a.x + (int64_t)(b0 + s_list[i]) * a.row_bytes,
+                          bytes, &bars[st]);
+            };
+            for (; issued < min(n, S - 1); ++issued) load(issued);
+            for (; landed < n; ++landed) {
+                const uint32_t r = seq + landed, st = r % S;
+                if (!mbar_wait_bounded(&bars[st], (r / S) & 1u, kTmaWaitLimit)) {
+                    report(a.status, EPD_ERR_TIMEOUT);
+                    s_failed = 1;
+                    break;
+                }
+                fence_proxy_async_smem();
+                const int *sl = s_slot + s_list[landed] * a.k;
+                for (int j = 0; j < a.k; ++j)
+                    if (sl[j] >= 0)
+                        bulk_store(a.out + (int64_t)sl[j] * a.row_bytes, stage + st * L.row_stride,
+                                   bytes);
+                bulk_commit();
+                if (issued < n) {
+                    bulk_wait_read<1>();  // the stage of row r - 1 is free again
+                    load(issued++);
+                }
+            }
+            if (s_failed) {  // let every load still in flight land before the block exits
+                for (int i = landed; i < issued; ++i) {
+                    const uint32_t r = seq + i;
+                    mbar_wait_bounded(&bars[r % S], (r / S) & 1u, kTmaWaitLimit);
+                }
+            }
+            seq += issued;
+            bulk_wait_read<0>();  // stages are reused by the next batch
+        } else if (a.scale_cols > 0) {
+            // fp8 scale rows with plain loads and stores, while thread 0 streams rows
+            const int nthreads = kTmaThreads - 32;
+            const int t2 = tid - 32;
+            if (t2 >= 0) {
+                for (int i = t2; i < nb * a.scale_cols; i += nthreads) {
+                    const int tl = i / a.scale_cols, c = i - tl * a.scale_cols;
+                    const float sv = a.x_scale[(int64_t)(b0 + tl) * a.scale_cols + c];
+                    for (int j = 0; j < a.k; ++j) {
+                        const int sl = s_slot[tl * a.k + j];
+                        if (sl >= 0) a.out_scale[(int64_t)sl * a.scale_cols + c] = sv;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (s_failed) break;
+    }
+    if (tid == 0) bulk_wait_all();
+
+    // rows [P, capacity) hold no pair
+    const int64_t stride = (int64_t)gridDim.x * kTmaThreads;
+    for (int64_t s = s_P + (int64_t)blockIdx.x * kTmaThreads + tid; s < a.capacity; s += stride)
+        a.m_indices[s] = -1;
+}
+
 }  // namespace
 }  // namespace epd
 
@@ -180,11 +335,35 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
     a.output_index = output_index;
     a.status = status;
 
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // bulk-copy kernel when at least two row stages fit in shared memory
+    const TmaSmem L = tma_smem(row_bytes, k);
+    if (L.stages >= 2) {
+        static size_t opted = 0;
+        if (L.total > opted) {
+            int dev = 0, optin = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                    cudaSuccess)
+                return record_cuda_error();
+            if (L.total + 64 <= (size_t)optin) {
+                if (cudaFuncSetAttribute(permute_tma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L.total) != cudaSuccess)
+                    return record_cuda_error();
+                opted = L.total;
+            }
+        }
+        if (L.total <= opted) {
+            const int grid = (int)(T < sm_count() ? (T < 1 ? 1 : T) : sm_count());
+            return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
+        }
+    }
     static int resident = 0;
     if (resident == 0) resident = blocks_per_sm(permute_kernel, kThreads, 0);
     const int64_t units = (int64_t)T * ((row_bytes / 16 + kUnitVecs - 1) / kUnitVecs);
     const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = (int64_t)sm_count() * resident;
     const int grid = (int)(want < 1 ? 1 : (want < full ? want : full));
-    return launch_pdl(permute_kernel, grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream), a);
+    return launch_pdl(permute_kernel, grid, kThreads, 0, cs, a);
 }
