@@ -65,8 +65,11 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     extern __shared__ int4 smem_raw[];
     unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);  // ranks
     unsigned long long *tok_nmask = tok_rmask + kLayoutMaxTileTokens;                 // nodes
-    int *hw = reinterpret_cast<int *>(tok_nmask + kLayoutMaxTileTokens);  // [W][E] -> warp bases
-    int *col_agg = hw + W * a.E;           // [cols_pad] this tile's counts
+    // [W][E + 1] warp histograms -> warp bases; rows padded by one word so that the
+    // per-expert scan across warps (stride of one row) hits 32 different banks
+    const int hws = a.E + 1;
+    int *hw = reinterpret_cast<int *>(tok_nmask + kLayoutMaxTileTokens);
+    int *col_agg = hw + W * hws;           // [cols_pad] this tile's counts
     int *col_excl = col_agg + a.cols_pad;  // [cols_pad] counts of earlier tiles
     int *rank_of = col_excl + a.cols_pad;  // [E] simulated rank of each expert
     int *node_of = rank_of + a.E;          // [R] simulated node of each rank
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     __shared__ int s_red[W];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < W * a.E; i += kThreads) hw[i] = 0;
+    for (int i = tid; i < W * hws; i += kThreads) hw[i] = 0;
     for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         pe[c] = (v >= 0 && v < a.E) ? (int)v : -1;
         if (v < -1 || v >= a.E) report(a.status, EPD_ERR_INVALID_EXPERT);
     }
-    int *my_hist = hw + warp * a.E;
+    int *my_hist = hw + warp * hws;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int e = pe[c];
@@ -180,14 +183,14 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     // (2) exclusive scan of the warp histograms per expert (warp-shuffle scan over
     // the W warps), and the tile's count per expert
     for (int e = warp; e < a.E; e += W) {
-        const int v = lane < W ? hw[lane * a.E + e] : 0;
+        const int v = lane < W ? hw[lane * hws + e] : 0;
         int incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int n = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += n;
         }
-        if (lane < W) hw[lane * a.E + e] = incl - v;
+        if (lane < W) hw[lane * hws + e] = incl - v;
         if (lane == 31) col_agg[e] = incl;
     }
     // (3b) tokens per rank and per node from the masks: one thread per
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     }
 
     // (7) rank of every pair inside its expert over the whole batch
-    const int *my_base = hw + warp * a.E;
+    const int *my_base = hw + warp * hws;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int p = p_base + 32 * c;
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
 
 size_t layout_smem_bytes(int E, int cols_pad) {
     return 2 * (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
-           ((size_t)layout_warps(E) * E + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int);
+           ((size_t)layout_warps(E) * (E + 1) + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int);
 }
 
 template <int W>
