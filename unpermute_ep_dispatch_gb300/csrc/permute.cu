@@ -46,7 +46,6 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     __shared__ int s_ok, s_P;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();  // offsets and pair ranks come from the previous kernels
-    pdl_trigger();
     if (threadIdx.x == 0) {
         const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
         s_ok = ok;
@@ -115,6 +114,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
         }
     }
 
+    // the next kernel may be scheduled now: triggering only after the row copies keeps
+    // its blocks from holding SM resources while this kernel streams
+    pdl_trigger();
     // rows [P, capacity) hold no pair
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t s = s_P + (int64_t)blockIdx.x * kThreads + threadIdx.x; s < a.capacity; s += stride)
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
 // small fp8 scale rows. The row copies run on the TMA engine instead of the
 // load/store units, whose store queue limits the register variant above.
 constexpr int kTmaThreads = 256;
-constexpr size_t kTmaStageBudget = 192 * 1024;  // shared memory for row stages
+constexpr size_t kTmaStageBudget = 64 * 1024;  // shared memory for row stages (a few blocks per SM)
 constexpr int kTmaMaxStages = 16;
 constexpr uint32_t kTmaWaitLimit = 1u << 24;    // mbarrier polls before a wait gives up
 
@@ -166,7 +168,6 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     uint64_t *bars = reinterpret_cast<uint64_t *>(tsm + L.bars_off);
     const int tid = threadIdx.x;
     pdl_wait();  // offsets and pair ranks come from the previous kernels
-    pdl_trigger();
     if (tid == 0) {
         const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
         s_ok = ok;
@@ -270,6 +271,9 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     }
     if (tid == 0) bulk_wait_all();
 
+    // the next kernel may be scheduled now: triggering only after the row copies keeps
+    // its blocks from holding SM resources while this kernel streams
+    pdl_trigger();
     // rows [P, capacity) hold no pair
     const int64_t stride = (int64_t)gridDim.x * kTmaThreads;
     for (int64_t s = s_P + (int64_t)blockIdx.x * kTmaThreads + tid; s < a.capacity; s += stride)
@@ -355,7 +359,8 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
             }
         }
         if (L.total <= opted) {
-            const int grid = (int)(T < sm_count() ? (T < 1 ? 1 : T) : sm_count());
+            // three blocks' worth of token runs per SM (measured best on GB300)
+            const int grid = (int)(T < 3 * sm_count() ? (T < 1 ? 1 : T) : 3 * sm_count());
             return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
         }
     }
