@@ -69,6 +69,8 @@ def _load():
         lib.oracle_dispatch_layout.restype = I
         lib.oracle_scan_offsets.argtypes = [P, I, P, P]
         lib.oracle_scan_offsets.restype = I
+        lib.oracle_scan_offsets_aligned.argtypes = [P, I, I, P, P]
+        lib.oracle_scan_offsets_aligned.restype = I
         lib.oracle_permute.argtypes = [P, I64, P, I, P, I, I, I, P, I64, P, P, P, P]
         lib.oracle_permute.restype = I
         lib.oracle_unpermute.argtypes = [P, I64, P, P, I, I, I, P]
@@ -121,6 +123,23 @@ def scan_offsets(tokens_per_expert):
     return start, int(total[0])
 
 
+def scan_offsets_aligned(tokens_per_expert, alignment: int):
+    """Returns (expert_start_loc [E] i32 of the padded regions, total padded rows)."""
+    cnt = _c(tokens_per_expert, np.int32)
+    start = np.zeros(cnt.shape[0], np.int32)
+    total = np.zeros(1, np.int32)
+    _check(_load().oracle_scan_offsets_aligned(_ptr(cnt), cnt.shape[0], int(alignment),
+                                               _ptr(start), _ptr(total)), "scan_offsets_aligned")
+    return start, int(total[0])
+
+
+def aligned_capacity(T: int, k: int, E: int, alignment: int) -> int:
+    """Rows that always suffice for padded regions: round_up(T*k + E*(alignment-1),
+    alignment) -- the upper bound of vLLM's compute_aligned_M."""
+    a = int(alignment)
+    return (T * k + E * (a - 1) + a - 1) // a * a
+
+
 def permute(x_rows, x_scale, topk_idx, num_experts: int, expert_start_loc, capacity: int):
     """x_rows: [T, row_bytes] uint8 (the raw bytes of each token row, any dtype);
     x_scale: [T, C] float32 or None. Returns dict(out [capacity, row_bytes] u8,
@@ -168,16 +187,19 @@ def double_from_bf16(b: int) -> float:
 
 
 def run_path(x_rows, x_scale, topk_idx, topk_weights, num_experts, num_ranks, num_rdma_ranks,
-             capacity=None, expert_out=None):
+             capacity=None, expert_out=None, alignment=1):
     """The whole path: layout -> offsets -> permute -> combine.
     expert_out: [capacity, H] uint16 bf16 bits, or None for identity experts
     (the permuted rows themselves, which must then be bf16)."""
     topk = _c(topk_idx, np.int64)
     T, k = topk.shape
     if capacity is None:
-        capacity = T * k
+        capacity = T * k if alignment == 1 else aligned_capacity(T, k, num_experts, alignment)
     lay = dispatch_layout(topk, num_experts, num_ranks, num_rdma_ranks)
-    start, total = scan_offsets(lay["tokens_per_expert"])
+    if alignment == 1:
+        start, total = scan_offsets(lay["tokens_per_expert"])
+    else:
+        start, total = scan_offsets_aligned(lay["tokens_per_expert"], alignment)
     per = permute(x_rows, x_scale, topk, num_experts, start, capacity)
     if expert_out is None:
         eo = per["out"].view(np.uint16)

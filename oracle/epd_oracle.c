@@ -128,6 +128,28 @@ int oracle_scan_offsets(const int32_t *tokens_per_expert, int E, int32_t *expert
 }
 
 /*
+ * Aligned expert offsets -- [P1] 3.3 / 4 (deepgemm_moe_permute and
+ * compute_aligned_M: every expert's rows are padded to a multiple of the
+ * alignment, block_m = 256, so the grouped GEMM sees whole blocks) and [P3]
+ * "Dispatch" (the dispatch docstring's expert_alignment: "align the number of
+ * tokens received by each local expert"): expert e's region holds
+ * round_up(count[e], alignment) rows, regions follow each other in expert
+ * order; *total = sum of the padded counts. alignment = 1 is the plain scan.
+ */
+int oracle_scan_offsets_aligned(const int32_t *tokens_per_expert, int E, int alignment,
+                                int32_t *expert_start_loc, int32_t *total) {
+    if (E < 1 || alignment < 1) return ORC_ERR_INVALID_ARG;
+    int64_t run = 0;
+    for (int e = 0; e < E; ++e) {
+        expert_start_loc[e] = (int32_t)run;
+        int64_t c = tokens_per_expert[e];
+        run += (c + alignment - 1) / alignment * alignment;
+    }
+    *total = (int32_t)run;
+    return ORC_OK;
+}
+
+/*
  * Permute (ep_scatter) -- [P1] 2.2 and 3.3: each token row (and its fp8 scale
  * row) is copied, byte for byte, to one row of the expert-contiguous buffer per
  * selected expert; m_indices[row] = expert of that row, output_index[t, j] =
@@ -147,7 +169,7 @@ int oracle_permute(const uint8_t *x, int64_t row_bytes, const float *x_scale, in
     if (T < 0 || k < 0 || E < 1 || row_bytes < 0 || capacity < 0) return ORC_ERR_INVALID_ARG;
     int32_t fill_count[E];
     for (int e = 0; e < E; ++e) fill_count[e] = 0;
-    int64_t filled = 0;
+    for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;
     for (int t = 0; t < T; ++t) {
         for (int j = 0; j < k; ++j) {
             int64_t e = topk_idx[(int64_t)t * k + j];
@@ -165,10 +187,8 @@ int oracle_permute(const uint8_t *x, int64_t row_bytes, const float *x_scale, in
             if (x_scale != NULL && scale_cols > 0)
                 memcpy(out_scale + s * scale_cols, x_scale + (int64_t)t * scale_cols,
                        (size_t)scale_cols * sizeof(float));
-            filled += 1;
         }
     }
-    for (int64_t s = filled; s < capacity; ++s) m_indices[s] = -1;
     return ORC_OK;
 }
 

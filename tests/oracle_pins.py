@@ -62,60 +62,93 @@ def check_hand_example(orc):
     assert rows_to_token_ids(per["out"][:total]) == g["permuted_source_tokens"]
 
 
+def check_hand_example_aligned(orc):
+    g = load_golden("hand_example_aligned4.json")
+    topk = np.array(g["topk_idx"], np.int64)
+    T = topk.shape[0]
+    lay = orc.dispatch_layout(topk, g["E"], g["R"], g["N"])
+    start, total = orc.scan_offsets_aligned(lay["tokens_per_expert"], g["alignment"])
+    assert start.tolist() == g["expert_start_loc"]
+    assert total == g["total_rows"]
+    assert orc.aligned_capacity(T, g["k"], g["E"], g["alignment"]) == g["capacity"]
+    per = orc.permute(token_id_rows(T), None, topk, g["E"], start, g["capacity"])
+    assert per["output_index"].tolist() == g["output_index"]
+    mi = per["m_indices"]
+    assert mi[:20].tolist() == g["m_indices_first_20"]
+    assert np.all(mi[20:] == -1)
+    src = rows_to_token_ids(per["out"])
+    for row, tok in g["permuted_source_tokens_by_row"].items():
+        assert src[int(row)] == tok
+
+
 # ----------------------------------------------------------------------------- independent definition
-def reference_by_sort(topk, E, R, N):
+def reference_by_sort(topk, E, R, N, alignment=1, capacity=None):
     """Layout and slots from an independent formulation: sort all valid pairs by
-    (expert, token, slot) -- the buffer is then read off in order."""
+    (expert, token, slot); walking the sorted list, an expert's first pair opens a
+    region at the next multiple of the alignment, and the buffer is read off."""
     T, k = topk.shape
     pairs = [(int(topk[t, j]), t, j) for t in range(T) for j in range(k) if topk[t, j] >= 0]
     order = sorted(pairs)
-    slot = {(t, j): s for s, (e, t, j) in enumerate(order)}
-    output_index = [[slot.get((t, j), -1) for j in range(k)] for t in range(T)]
-    m_indices = [e for (e, _, _) in order] + [-1] * (T * k - len(order))
     cnt = Counter(e for (e, _, _) in order)
     counts = [cnt.get(e, 0) for e in range(E)]
+    if capacity is None:
+        capacity = T * k
+    slot, m_indices, row, prev = {}, [-1] * capacity, 0, None
+    for (e, t, j) in order:
+        if e != prev:
+            row = -(-row // alignment) * alignment      # next region starts aligned
+            prev = e
+        slot[(t, j)] = row
+        m_indices[row] = e
+        row += 1
+    output_index = [[slot.get((t, j), -1) for j in range(k)] for t in range(T)]
+    start = []
+    acc = 0
+    for e in range(E):
+        start.append(acc)
+        acc += -(-counts[e] // alignment) * alignment
+    total_aligned = acc
     epr = E // R
     rpn = R // N
     token_ranks = [{int(e) // epr for e in topk[t] if e >= 0} for t in range(T)]
     token_nodes = [{r // rpn for r in rs} for rs in token_ranks]
     per_rank = [sum(r in rs for rs in token_ranks) for r in range(R)]
     per_node = [sum(n in ns for ns in token_nodes) for n in range(N)]
-    first = {}
-    for s, (e, _, _) in enumerate(order):
-        first.setdefault(e, s)
-    # start of an expert = number of pairs of lower experts
-    start = [sum(counts[:e]) for e in range(E)]
     return dict(output_index=output_index, m_indices=m_indices, counts=counts, start=start,
-                per_rank=per_rank, per_node=per_node, token_ranks=token_ranks, total=len(order))
+                per_rank=per_rank, per_node=per_node, token_ranks=token_ranks,
+                total=len(order) if alignment == 1 else total_aligned, slot=slot)
 
 
-def check_against_sort(orc, topk, E, R, N):
+def check_against_sort(orc, topk, E, R, N, alignment=1):
     T, k = topk.shape
-    ref = reference_by_sort(topk, E, R, N)
+    cap = T * k if alignment == 1 else orc.aligned_capacity(T, k, E, alignment)
+    ref = reference_by_sort(topk, E, R, N, alignment, cap)
     lay = orc.dispatch_layout(topk, E, R, N)
     assert lay["tokens_per_expert"].tolist() == ref["counts"], "counts"
     assert lay["tokens_per_rank"].tolist() == ref["per_rank"], "per_rank"
     assert lay["tokens_per_rdma_rank"].tolist() == ref["per_node"], "per_node"
     sets = [set(np.nonzero(row)[0].tolist()) for row in lay["is_token_in_rank"]]
     assert sets == ref["token_ranks"], "is_token_in_rank"
-    start, total = orc.scan_offsets(lay["tokens_per_expert"])
+    if alignment == 1:
+        start, total = orc.scan_offsets(lay["tokens_per_expert"])
+    else:
+        start, total = orc.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
     assert start.tolist() == ref["start"], "start"
     assert total == ref["total"], "total"
     x = token_id_rows(T)
-    per = orc.permute(x, None, topk, E, start, T * k)
+    per = orc.permute(x, None, topk, E, start, cap)
     assert per["output_index"].tolist() == ref["output_index"], "output_index"
     assert per["m_indices"].tolist() == ref["m_indices"], "m_indices"
-    src = rows_to_token_ids(per["out"][:total])
-    for s, (e, t, j) in enumerate(sorted((int(topk[t, j]), t, j) for t in range(T)
-                                         for j in range(k) if topk[t, j] >= 0)):
-        assert src[s] == t, "permuted row source"
+    src = rows_to_token_ids(per["out"])
+    for (t, j), row in ref["slot"].items():
+        assert src[row] == t, "permuted row source"
 
 
-def check_bruteforce(orc, T, k, E, R, N, limit=None):
+def check_bruteforce(orc, T, k, E, R, N, limit=None, alignment=1):
     """Every topk_idx in {-1..E-1}^(T x k) (with repeats) against the sort definition."""
     n = 0
     for flat in itertools.product(range(-1, E), repeat=T * k):
-        check_against_sort(orc, np.array(flat, np.int64).reshape(T, k), E, R, N)
+        check_against_sort(orc, np.array(flat, np.int64).reshape(T, k), E, R, N, alignment)
         n += 1
         if limit is not None and n >= limit:
             break
@@ -123,21 +156,30 @@ def check_bruteforce(orc, T, k, E, R, N, limit=None):
 
 
 # ----------------------------------------------------------------------------- invariants
-def check_invariants(orc, topk, E, R, N, row_bytes=32, with_scale=True, capacity=None):
+def check_invariants(orc, topk, E, R, N, row_bytes=32, with_scale=True, capacity=None,
+                     alignment=1):
     T, k = topk.shape
     if capacity is None:
-        capacity = T * k
+        capacity = T * k if alignment == 1 else orc.aligned_capacity(T, k, E, alignment)
     valid = topk >= 0
     P = int(valid.sum())
     lay = orc.dispatch_layout(topk, E, R, N)
     cnt = lay["tokens_per_expert"].astype(np.int64)
     assert cnt.sum() == P                                    # counts sum to the valid picks
-    start, total = orc.scan_offsets(lay["tokens_per_expert"])
-    assert total == P
+    if alignment == 1:
+        start, total = orc.scan_offsets(lay["tokens_per_expert"])
+        assert total == P
+        padded = cnt
+    else:
+        start, total = orc.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
+        padded = -(-cnt // alignment) * alignment
+        assert np.all(start % alignment == 0)                # regions start aligned
+        assert total <= capacity                             # compute_aligned_M bound holds
+        assert total == padded.sum()
     if E > 0:
         assert start[0] == 0
-        assert np.all(np.diff(start.astype(np.int64)) == cnt[:-1])   # offsets tile [0, P)
-        assert int(start[-1]) + int(cnt[-1]) == P
+        assert np.all(np.diff(start.astype(np.int64)) == padded[:-1])  # regions tile [0, total)
+        assert int(start[-1]) + int(padded[-1]) == total
     rng = np.random.default_rng(T * 131 + k)
     x = rng.integers(0, 256, size=(T, row_bytes), dtype=np.uint8)
     sc = rng.standard_normal((T, 3)).astype(np.float32) if with_scale else None
@@ -146,9 +188,13 @@ def check_invariants(orc, topk, E, R, N, row_bytes=32, with_scale=True, capacity
     mi = per["m_indices"]
     assert np.all(oi[~valid] == -1)
     slots = oi[valid]
-    assert sorted(slots.tolist()) == list(range(P))         # bijection onto [0, P)
+    filled = np.concatenate([np.arange(start[e], start[e] + cnt[e]) for e in range(E)]) \
+        if E else np.zeros(0, np.int64)
+    assert sorted(slots.tolist()) == sorted(filled.tolist())  # bijection onto the filled rows
     assert np.all(mi[slots] == topk[valid])                  # row -> expert
-    assert np.all(mi[P:] == -1)
+    empty = np.ones(capacity, bool)
+    empty[slots] = False
+    assert np.all(mi[empty] == -1)                           # padding and tail rows
     assert np.array_equal(per["out"][slots], np.repeat(x, k, axis=0)[valid.reshape(-1)])
     if with_scale:
         assert np.array_equal(per["out_scale"][slots], np.repeat(sc, k, axis=0)[valid.reshape(-1)])

@@ -10,7 +10,7 @@ import pytest
 
 import oracle as oracle_pkg
 from oracle_pins import (check_bf16_rounding, check_bruteforce, check_combine_all,
-                         check_hand_example, check_invariants)
+                         check_hand_example, check_hand_example_aligned, check_invariants)
 
 SRC = os.path.join(os.path.dirname(oracle_pkg.__file__), "epd_oracle.c")
 
@@ -22,8 +22,12 @@ MUTANTS = {
     "pairs_not_tokens": ("in_rank = 1;", "in_rank += 1;"),
     "dropped_fill_increment": ("fill_count[e] += 1;", ""),
     "m_indices_wrong_operand": ("m_indices[s] = (int32_t)e;", "m_indices[s] = (int32_t)t;"),
-    "tail_off_by_one": ("for (int64_t s = filled; s < capacity; ++s)",
-                        "for (int64_t s = filled + 1; s < capacity; ++s)"),
+    "unfilled_rows_not_cleared": ("for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;", ""),
+    "first_row_not_cleared": ("for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;",
+                              "for (int64_t s = 1; s < capacity; ++s) m_indices[s] = -1;"),
+    "alignment_rounds_down": ("run += (c + alignment - 1) / alignment * alignment;",
+                              "run += c / alignment * alignment;"),
+    "alignment_ignored": ("run += (c + alignment - 1) / alignment * alignment;", "run += c;"),
     "weight_wrong_index": ("acc += (double)topk_weights[(int64_t)t * k + j] *",
                            "acc += (double)topk_weights[(int64_t)t * k] *"),
     "combine_wrong_sign": ("acc += (double)topk_weights", "acc -= (double)topk_weights"),
@@ -51,6 +55,8 @@ def _load_mutant(tmp_path, name):
 
 def _run_pins(orc):
     check_hand_example(orc)
+    check_hand_example_aligned(orc)
+    check_bruteforce(orc, 2, 2, 4, 2, 1, limit=2000, alignment=4)
     check_bruteforce(orc, 3, 2, 4, 2, 1, limit=3000)
     check_bruteforce(orc, 2, 2, 4, 4, 2, limit=3000)
     rng = np.random.default_rng(0)

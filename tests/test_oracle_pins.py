@@ -6,7 +6,7 @@ import torch
 import oracle
 from oracle_pins import (check_against_sort, check_bf16_rounding, check_bruteforce,
                          check_combine_exact_sums, check_combine_identity, check_combine_one_hot,
-                         check_hand_example, check_invariants)
+                         check_hand_example, check_hand_example_aligned, check_invariants)
 from unpermute_ep_dispatch_gb300 import workloads
 
 
@@ -113,3 +113,34 @@ def test_combine_identity_on_prefill_shape():
     has = (c.topk_idx >= 0).any(dim=1).numpy()
     assert np.array_equal(res["y"][has], xb[has])
     assert np.all(res["y"][~has] == 0)
+
+
+# ----------------------------------------------------------------------------- expert alignment
+def test_hand_example_aligned():
+    """The worked routing with every expert padded to a multiple of 4."""
+    check_hand_example_aligned(oracle)
+
+
+@pytest.mark.parametrize("T,k,E,R,N,alignment", [
+    (3, 2, 4, 2, 1, 2), (3, 2, 4, 4, 2, 4), (2, 2, 3, 3, 1, 3), (1, 4, 4, 2, 2, 8),
+])
+def test_bruteforce_tiny_aligned(T, k, E, R, N, alignment):
+    n = check_bruteforce(oracle, T, k, E, R, N, alignment=alignment)
+    assert n == (E + 1) ** (T * k)
+
+
+@pytest.mark.parametrize("alignment", [2, 16, 128, 256])
+def test_invariants_aligned(alignment):
+    c = workloads.make_case("dsv3_fp8", T=300)
+    check_invariants(oracle, c.topk_idx.numpy(), c.E, c.R, c.N, alignment=alignment)
+    rng = np.random.default_rng(alignment)
+    topk = rng.integers(-1, 16, size=(77, 5)).astype(np.int64)
+    check_invariants(oracle, topk, 16, 4, 2, alignment=alignment)
+
+
+def test_alignment_one_is_the_plain_scan():
+    rng = np.random.default_rng(3)
+    cnt = rng.integers(0, 50, size=64).astype(np.int32)
+    a, ta = oracle.scan_offsets_aligned(cnt, 1)
+    b, tb = oracle.scan_offsets(cnt)
+    assert a.tolist() == b.tolist() and ta == tb
