@@ -75,6 +75,7 @@ typedef enum {
 
 #define EPD_MAX_EXPERTS 4096
 #define EPD_MAX_TOPK 64
+#define EPD_MAX_ALIGNMENT 4096
 
 /* Human-readable name of a status code (static string; never NULL). */
 EPD_API const char *epd_status_string(int code);
@@ -144,6 +145,22 @@ EPD_API epd_status_t ep_scan_offsets(const int32_t *tokens_per_expert, int num_e
                              epd_stream_t stream);
 
 /*
+ * Step 2 with expert alignment (the grouped-GEMM contiguous layout). [P1] 3.3
+ * and 4 (deepgemm_moe_permute pads every expert to block_m = 256 rows;
+ * compute_aligned_M) and [P3] "Dispatch" (dispatch's expert_alignment): every
+ * expert's region holds round_up(tokens_per_expert[e], alignment) rows;
+ * expert_start_loc[e] = sum of the padded counts of e' < e, *total_rows = the sum
+ * of all padded counts. alignment in [1, EPD_MAX_ALIGNMENT]; 1 gives
+ * ep_scan_offsets. A buffer of round_up(T*k + E*(alignment-1), alignment) rows
+ * always holds the padded regions. ep_permute fills them and marks the padding
+ * rows with m_indices = -1.
+ */
+EPD_API epd_status_t ep_scan_offsets_aligned(const int32_t *tokens_per_expert, int num_experts,
+                                             int alignment, int32_t *expert_start_loc,
+                                             int32_t *total_rows, int32_t *status,
+                                             epd_stream_t stream);
+
+/*
  * Step 3 -- permute (ep_scatter). [P1] 2.2 (ep_scatter into input_tensor,
  * input_tensor_scale, m_indices, output_index) and 3.3 (m_indices pre-set to
  * -1 so that unwritten rows are skipped): for every pair (t, j) with expert
@@ -154,14 +171,17 @@ EPD_API epd_status_t ep_scan_offsets(const int32_t *tokens_per_expert, int num_e
  *   m_indices[s]      = e,
  *   output_index[t,j] = s;
  * pairs with no selection get output_index = -1, and m_indices[s] = -1 for
- * every s in [P, capacity_rows), P = number of valid pairs. Rows of out and
- * out_scale at and beyond P are not written.
+ * every row s in [0, capacity_rows) that no pair fills (alignment padding and
+ * the rows after the last region). expert_start_loc may come from
+ * ep_scan_offsets or ep_scan_offsets_aligned. Rows of out and out_scale that no
+ * pair fills are not written.
  *   x:            [T, H] dtype rows, 16-byte aligned;
  *   x_scale:      [T, H/128] float32 for EPD_FP8_E4M3, NULL for EPD_BF16;
  *   out:          [capacity_rows, H] dtype, 16-byte aligned;
  *   out_scale:    [capacity_rows, H/128] float32 (fp8) or NULL (bf16);
  *   m_indices:    [capacity_rows] int32;  output_index: [T, k] int32;
- *   capacity_rows >= T*k (the exact-allocation upper bound with alignment 1),
+ *   capacity_rows >= T*k (the exact-allocation upper bound with alignment 1;
+ *   with aligned offsets it must also hold the padded regions),
  *   capacity_rows <= INT32_MAX.
  * `workspace` must hold the layout of the same topk_idx (same T and k); a
  * mismatch sets EPD_ERR_INVALID_ARG in *status and writes nothing.

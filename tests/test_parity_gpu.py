@@ -23,11 +23,11 @@ def _built():
     epd.load_library()
 
 
-def run_both(case, capacity=None, stream=None):
-    g = GpuPath(case, capacity=capacity, stream=stream)
+def run_both(case, capacity=None, stream=None, alignment=1):
+    g = GpuPath(case, capacity=capacity, stream=stream, alignment=alignment)
     g.step()
     got = g.results()
-    want = oracle_path(case, capacity=capacity)
+    want = oracle_path(case, capacity=capacity, alignment=alignment)
     return got, want, g
 
 
@@ -252,3 +252,40 @@ def test_cuda_graph_replay_of_the_step():
         torch.cuda.synchronize()
         graph.replay()
         compare(g.results(), oracle_path(case))
+
+
+# ----------------------------------------------------------------------------- expert alignment
+@pytest.mark.parametrize("alignment", [4, 128, 256])
+@pytest.mark.parametrize("name,T", [("tiny", None), ("dsv3_fp8", 2048), ("prefill_bf16", 1000),
+                                    ("skew_bf16", 2048)])
+def test_aligned_layouts(name, T, alignment):
+    case = workloads.make_case(name, T=T)
+    got, want, _ = run_both(case, alignment=alignment)
+    compare(got, want)
+    start = got["expert_start_loc"]
+    assert np.all(start % alignment == 0)
+
+
+def test_aligned_hand_example_on_gpu():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "hand_example_aligned4.json")))
+    topk = torch.tensor(g["topk_idx"], dtype=torch.int64)
+    case = workloads.make_random_case(T=4, H=64, k=2, E=16, R=8, N=2, dtype="bf16", seed=1,
+                                      routing="uniform", experts="random")
+    case = workloads.Case(**{**case.__dict__, "topk_idx": topk})
+    got, want, _ = run_both(case, alignment=4)
+    compare(got, want)
+    assert got["expert_start_loc"].tolist() == g["expert_start_loc"]
+    assert got["output_index"].tolist() == g["output_index"]
+    assert got["m_indices"][:20].tolist() == g["m_indices_first_20"]
+
+
+@pytest.mark.parametrize("T", [0, 1, 33])
+@pytest.mark.parametrize("p_invalid", [0.0, 0.5, 1.0])
+def test_aligned_edges(T, p_invalid):
+    case = workloads.make_random_case(T=T, H=128, k=8, E=16, R=4, N=2, dtype="fp8", seed=T + 7,
+                                      routing="repeats", p_invalid=p_invalid, experts="random")
+    got, want, _ = run_both(case, alignment=64)
+    compare(got, want)

@@ -42,6 +42,7 @@ SIGNATURES = {
     "epd_workspace_init": (_I, [_P, _SZ, _P]),
     "ep_dispatch_layout": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "ep_scan_offsets": (_I, [_P, _I, _P, _P, _P, _P]),
+    "ep_scan_offsets_aligned": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "ep_permute": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "ep_unpermute": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _P]),
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -207,6 +208,30 @@ def ep_scan_offsets(tokens_per_expert: torch.Tensor, status: torch.Tensor,
                                         _ptr(status), _stream(stream, dev))
     _check(rc, "ep_scan_offsets")
     return start, total
+
+
+def ep_scan_offsets_aligned(tokens_per_expert: torch.Tensor, alignment: int,
+                            status: torch.Tensor, expert_start_loc=None, total_rows=None,
+                            stream=None):
+    """Step 2 with every expert's region padded to a multiple of `alignment`.
+    Returns (expert_start_loc [E] i32, total_rows [1] i32), both on the device."""
+    _want(tokens_per_expert, "tokens_per_expert", torch.int32)
+    dev = tokens_per_expert.device
+    E = tokens_per_expert.numel()
+    _want(status, "status", torch.int32, (1,), dev)
+    start = _out(expert_start_loc, "expert_start_loc", torch.int32, (E,), dev)
+    total = _out(total_rows, "total_rows", torch.int32, (1,), dev)
+    rc = load_library().ep_scan_offsets_aligned(_ptr(tokens_per_expert), E, int(alignment),
+                                                _ptr(start), _ptr(total), _ptr(status),
+                                                _stream(stream, dev))
+    _check(rc, "ep_scan_offsets_aligned")
+    return start, total
+
+
+def aligned_capacity(num_tokens: int, num_topk: int, num_experts: int, alignment: int) -> int:
+    """Rows that always hold the padded regions: round_up(T*k + E*(alignment-1), alignment)."""
+    a = int(alignment)
+    return (num_tokens * num_topk + num_experts * (a - 1) + a - 1) // a * a
 
 
 def ep_permute(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: torch.Tensor,

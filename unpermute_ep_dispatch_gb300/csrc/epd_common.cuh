@@ -47,11 +47,16 @@ __host__ __device__ inline int layout_tile_tokens(int k) {
 }
 
 struct WsLayout {
-    size_t header_off, pair_rank_off, state_off, agg_off, incl_off, total;
+    size_t header_off, pair_rank_off, counts_off, state_off, agg_off, incl_off, total;
     int tiles, cols, cols_pad;
 };
 
 __host__ __device__ inline size_t ws_pair_rank_off() { return kAlign; }
+
+// The layout's per-expert counts, kept for ep_permute (which needs T, k and E only).
+__host__ __device__ inline size_t ws_counts_off(int T, int k) {
+    return align_up(kAlign + (size_t)T * (size_t)k * 4, kAlign);
+}
 
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N) {
     WsLayout w;
@@ -61,7 +66,8 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N)
     w.cols_pad = (int)align_up((size_t)w.cols, 32);
     w.header_off = 0;
     w.pair_rank_off = ws_pair_rank_off();
-    w.state_off = align_up(w.pair_rank_off + (size_t)T * (size_t)k * 4, kAlign);
+    w.counts_off = ws_counts_off(T, k);
+    w.state_off = align_up(w.counts_off + (size_t)E * 4, kAlign);
     w.agg_off = align_up(w.state_off + (size_t)w.tiles * 4, kAlign);
     w.incl_off = align_up(w.agg_off + (size_t)w.tiles * w.cols_pad * 4, kAlign);
     w.total = align_up(w.incl_off + (size_t)w.tiles * w.cols_pad * 4, kAlign);

@@ -43,6 +43,7 @@ struct LayoutArgs {
     uint8_t *in_rank;
     WsHeader *hdr;
     int32_t *pair_rank;
+    int32_t *ws_counts;
     uint32_t *state;
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
             const int tot = col_excl[c] + col_agg[c];
             if (c < a.E) {
                 a.per_expert[c] = tot;
+                a.ws_counts[c] = tot;
                 part += tot;
             } else if (c < a.E + a.R) {
                 a.per_rank[c - a.E] = tot;
@@ -433,6 +435,7 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.in_rank = in_rank;
     a.hdr = reinterpret_cast<WsHeader *>(ws + w.header_off);
     a.pair_rank = reinterpret_cast<int32_t *>(ws + w.pair_rank_off);
+    a.ws_counts = reinterpret_cast<int32_t *>(ws + w.counts_off);
     a.state = reinterpret_cast<uint32_t *>(ws + w.state_off);
     a.agg = reinterpret_cast<int32_t *>(ws + w.agg_off);
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);

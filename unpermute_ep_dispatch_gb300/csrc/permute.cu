@@ -32,6 +32,7 @@ struct PermuteArgs {
     int T, k, E;
     const int32_t *start;
     const int32_t *pair_rank;
+    const int32_t *counts;  // per-expert counts the layout left in the workspace
     const WsHeader *hdr;
     int64_t capacity;
     uint8_t *out;
@@ -41,15 +42,32 @@ struct PermuteArgs {
     int32_t *status;
 };
 
+// m_indices over the whole buffer from the expert segments: row s belongs to the
+// last expert whose region starts at or before s (experts that share a start have
+// empty regions), and holds that expert when it is among the region's first
+// count rows, else -1 (alignment padding, or rows after the last region). Works
+// for plain and aligned offsets alike; coalesced, one binary search per row.
+__device__ __forceinline__ void fill_m_indices(const PermuteArgs &a, int64_t first, int64_t stride) {
+    for (int64_t s = first; s < a.capacity; s += stride) {
+        int lo = 0, hi = a.E - 1;
+        while (lo < hi) {  // last e with start[e] <= s
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)__ldg(a.start + mid) <= s) lo = mid;
+            else hi = mid - 1;
+        }
+        const int64_t st = __ldg(a.start + lo);
+        a.m_indices[s] = (s >= st && s < st + __ldg(a.counts + lo)) ? lo : -1;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     __shared__ int s_slot[kWarps][EPD_MAX_TOPK];
-    __shared__ int s_ok, s_P;
+    __shared__ int s_ok;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();  // offsets and pair ranks come from the previous kernels
     if (threadIdx.x == 0) {
         const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
         s_ok = ok;
-        s_P = ok ? max(0, a.hdr->total_pairs) : 0;
         if (!ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
     }
     __syncthreads();
@@ -80,10 +98,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
                     if (sl >= 0 && sl < a.capacity) s = (int)sl;
                     else if (ch == 0) report(a.status, EPD_ERR_CAPACITY);
                 }
-                if (ch == 0) {
-                    a.output_index[idx] = s;
-                    if (s >= 0) a.m_indices[s] = (int)e;
-                }
+                if (ch == 0) a.output_index[idx] = s;
                 s_slot[warp][j] = s;
                 has |= (s >= 0);
             }
@@ -117,10 +132,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    // rows [P, capacity) hold no pair
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t s = s_P + (int64_t)blockIdx.x * kThreads + threadIdx.x; s < a.capacity; s += stride)
-        a.m_indices[s] = -1;
+    fill_m_indices(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
 }
 
 // ----------------------------------------------------------------------------- bulk-copy variant
@@ -160,7 +172,7 @@ __host__ __device__ inline TmaSmem tma_smem(int64_t row_bytes, int k) {
 
 __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a) {
     extern __shared__ __align__(128) uint8_t tsm[];
-    __shared__ int s_ok, s_P, s_n, s_failed;
+    __shared__ int s_ok, s_n, s_failed;
     const TmaSmem L = tma_smem(a.row_bytes, a.k);
     uint8_t *stage = tsm;
     int *s_slot = reinterpret_cast<int *>(tsm + L.slots_off);  // [batch tokens][k]
@@ -171,7 +183,6 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     if (tid == 0) {
         const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
         s_ok = ok;
-        s_P = ok ? max(0, a.hdr->total_pairs) : 0;
         s_failed = 0;
         if (!ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
         for (int i = 0; i < L.stages; ++i) mbar_init(&bars[i], 1);
@@ -199,7 +210,6 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
                 const int64_t sl = (int64_t)a.start[e] + a.pair_rank[idx];
                 if (sl >= 0 && sl < a.capacity) {
                     s = (int)sl;
-                    a.m_indices[s] = (int)e;
                 } else {
                     report(a.status, EPD_ERR_CAPACITY);
                 }
@@ -274,10 +284,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    // rows [P, capacity) hold no pair
-    const int64_t stride = (int64_t)gridDim.x * kTmaThreads;
-    for (int64_t s = s_P + (int64_t)blockIdx.x * kTmaThreads + tid; s < a.capacity; s += stride)
-        a.m_indices[s] = -1;
+    fill_m_indices(a, (int64_t)blockIdx.x * kTmaThreads + tid, (int64_t)gridDim.x * kTmaThreads);
 }
 
 }  // namespace
@@ -331,6 +338,7 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
     a.E = E;
     a.start = expert_start_loc;
     a.pair_rank = reinterpret_cast<const int32_t *>(ws + ws_pair_rank_off());
+    a.counts = reinterpret_cast<const int32_t *>(ws + ws_counts_off(T, k));
     a.hdr = reinterpret_cast<const WsHeader *>(ws);
     a.capacity = capacity_rows;
     a.out = static_cast<uint8_t *>(out);
