@@ -260,7 +260,8 @@ def run_epd(args, rank, world, local):
     name = args.workload
     case = workloads.make_case(name, T=args.tokens)
     T, H, k, E, R, N = case.T, case.H, case.k, case.E, case.R, case.N
-    M = case.capacity
+    A = max(1, int(args.align))
+    M = case.capacity if A == 1 else epd.aligned_capacity(T, k, E, A)
     stream = torch.cuda.Stream(dev)
 
     # device-resident inputs and outputs (allocated once; the step allocates nothing)
@@ -290,8 +291,10 @@ def run_epd(args, rank, world, local):
             lambda: epd.ep_dispatch_layout(topk, E, R, N, ws, status, tokens_per_expert=per_e,
                                            tokens_per_rank=per_r, tokens_per_rdma_rank=per_n,
                                            is_token_in_rank=itr, stream=stream),
-            lambda: epd.ep_scan_offsets(per_e, status, expert_start_loc=start, total_rows=total,
-                                        stream=stream),
+            (lambda: epd.ep_scan_offsets(per_e, status, expert_start_loc=start,
+                                         total_rows=total, stream=stream)) if A == 1 else
+            (lambda: epd.ep_scan_offsets_aligned(per_e, A, status, expert_start_loc=start,
+                                                 total_rows=total, stream=stream)),
             lambda: epd.ep_permute(x, xs, topk, E, start, ws, status, capacity_rows=M, out=out,
                                    out_scale=out_scale, m_indices=m_idx, output_index=out_idx,
                                    stream=stream),
@@ -310,7 +313,7 @@ def run_epd(args, rank, world, local):
         step()
     torch.cuda.synchronize(dev)
     epd.check_status(status, "warm-up")
-    P = int(total.item())
+    P = int((out_idx >= 0).sum().item())  # valid pairs
 
     names = ["ep_dispatch_layout", "ep_scan_offsets", "ep_permute", "ep_unpermute"]
     # the dominant kernel by algorithmic bytes carries events inside the timed region;
@@ -403,6 +406,8 @@ def run_epd(args, rank, world, local):
                "ep_dispatch_layout": "layout.cu", "ep_scan_offsets": "scan.cu"}[dom]
     achieved = bytes_k[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
     ms_per_step = ms / args.steps
+    P = int((out_idx >= 0).sum().item())        # valid pairs (total is the padded row count)
+    bytes_k = algorithmic_bytes(case, P, M)
     path_bytes = sum(bytes_k.values())
     path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
     kernels = {n: {"us": round(per_kernel_ms[n] * 1e3, 2), "bytes": bytes_k[n],
@@ -428,7 +433,7 @@ def run_epd(args, rank, world, local):
                    "rows": "fp8_e4m3 + f32 scale per 128 columns" if case.dtype == "fp8"
                    else "bf16",
                    "expert_out": "bf16 identity (permuted rows)" if eo is None else "bf16 seeded",
-                   "capacity_rows": M, "valid_pairs": P,
+                   "capacity_rows": M, "valid_pairs": P, "expert_alignment": A,
                    "l2": f"no flush: {path_bytes / 1e6:.0f} MB moved per step > 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "hbm": {"path_gbs": round(path_gbs, 1), "path_bytes": path_bytes,
@@ -662,6 +667,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--align", type=int, default=1,
+                    help="pad every expert's rows to a multiple of this (grouped-GEMM layout)")
     ap.add_argument("--decode-pool", type=int, default=16,
                     help="distinct input sets cycled by the decode workload")
     args = ap.parse_args(argv)
