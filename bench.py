@@ -270,6 +270,9 @@ def run_epd(args, rank, world, local):
     x = case.x.to(dev)
     xs = None if case.x_scale is None else case.x_scale.to(dev)
     eo = None if case.expert_out is None else case.expert_out.to(dev)
+    if eo is not None and M > eo.shape[0]:
+        # an aligned layout's expert outputs span every padded row: repeat the seeded rows
+        eo = torch.cat([eo, eo[: M - eo.shape[0]]])
     ws = epd.new_workspace(T, k, E, R, N, dev)
     status = epd.new_status(dev)
     per_e = torch.empty(E, dtype=torch.int32, device=dev)
@@ -363,7 +366,8 @@ def run_epd(args, rank, world, local):
     if not args.no_e2e:
         pin = lambda t: None if t is None else t.contiguous().pin_memory()  # noqa: E731
         h_topk, h_w, h_x, h_xs, h_eo = (pin(case.topk_idx), pin(case.topk_weights),
-                                        pin(case.x), pin(case.x_scale), pin(case.expert_out))
+                                        pin(case.x), pin(case.x_scale),
+                                        None if eo is None else pin(eo.cpu()))
         h_y = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in (h_topk, h_w, h_x, h_xs, h_eo)
                   if t is not None)
