@@ -73,6 +73,9 @@ def _load():
         lib.oracle_scan_offsets_aligned.restype = I
         lib.oracle_permute.argtypes = [P, I64, P, I, P, I, I, I, P, I64, P, P, P, P]
         lib.oracle_permute.restype = I
+        lib.oracle_permute_ex.argtypes = [P, I64, P, I, I, I64, P, I, I, I, I, I, P, I64, P, P, P,
+                                          P]
+        lib.oracle_permute_ex.restype = I
         lib.oracle_unpermute.argtypes = [P, I64, P, P, I, I, I, P]
         lib.oracle_unpermute.restype = I
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
@@ -161,6 +164,40 @@ def permute(x_rows, x_scale, topk_idx, num_experts: int, expert_start_loc, capac
                                 num_experts, _ptr(start), capacity, _ptr(out), _ptr(out_scale),
                                 _ptr(m_indices), _ptr(output_index))
     _check(rc, "permute")
+    return dict(out=out, out_scale=out_scale, m_indices=m_indices, output_index=output_index)
+
+
+def permute_ex(x_rows, x_scale_words, topk_idx, num_experts: int, expert_start_loc,
+               capacity: int, expert_begin: int = 0, expert_end=None, scale_col_major=False,
+               scale_ld=None):
+    """Permute with output options: only experts [expert_begin, expert_end) with local
+    rows and local ids (expert - expert_begin); scale rows of 32-bit words (fp32 or
+    UE8M0-packed) copied row-major or column-major with leading dimension scale_ld.
+    Returns dict(out, out_scale (uint32 words: [capacity, C] row-major or
+    [C, scale_ld] column-major) or None, m_indices, output_index)."""
+    xb = _c(x_rows, np.uint8)
+    topk = _c(topk_idx, np.int64)
+    T, k = topk.shape
+    E = num_experts
+    e_end = E if expert_end is None else expert_end
+    sc = None if x_scale_words is None else np.ascontiguousarray(x_scale_words).view(np.uint32)
+    C = 0 if sc is None else sc.shape[1]
+    ld = capacity if scale_ld is None else int(scale_ld)
+    start = _c(expert_start_loc, np.int32)
+    out = np.zeros((capacity, xb.shape[1]), np.uint8)
+    if sc is None:
+        out_scale = None
+    elif scale_col_major:
+        out_scale = np.zeros((C, ld), np.uint32)
+    else:
+        out_scale = np.zeros((capacity, C), np.uint32)
+    m_indices = np.zeros(capacity, np.int32)
+    output_index = np.zeros((T, k), np.int32)
+    rc = _load().oracle_permute_ex(_ptr(xb), xb.shape[1], _ptr(sc), C, int(bool(scale_col_major)),
+                                   ld, _ptr(topk), T, k, E, int(expert_begin), int(e_end),
+                                   _ptr(start), capacity, _ptr(out), _ptr(out_scale),
+                                   _ptr(m_indices), _ptr(output_index))
+    _check(rc, "permute_ex")
     return dict(out=out, out_scale=out_scale, m_indices=m_indices, output_index=output_index)
 
 

@@ -193,6 +193,60 @@ int oracle_permute(const uint8_t *x, int64_t row_bytes, const float *x_scale, in
 }
 
 /*
+ * Permute with output options -- the receiver-side view of one simulated rank
+ * and the scale layouts a grouped GEMM reads:
+ *   - local view ([P1] 3.1.2 and 7: after dispatch a rank holds its own experts
+ *     under local ids, expert - rank_expert_offset; [P1] 3.3 deepgemm_moe_permute
+ *     over local_num_experts): only pairs whose expert is in [e_begin, e_end)
+ *     are placed; the buffer starts at the region of e_begin, so a pair's row
+ *     is expert_start_loc[e] - expert_start_loc[e_begin] + its rank inside e;
+ *     m_indices holds the local id e - e_begin; other pairs get -1;
+ *   - scales ([P1] 2.2: input_tensor_scale [M, H/128], or for UE8M0 an int
+ *     tensor [ceil(H/512), M] viewed transposed; [P3] low_latency_dispatch
+ *     docstring: scales column-major for TMA): each token's scale row of
+ *     scale_cols 32-bit words (fp32 scales or packed UE8M0 bytes) is copied to
+ *     row s either row-major (out_scale[s * scale_cols + c]) or column-major
+ *     (out_scale[c * scale_ld + s]).
+ * Rows no pair fills keep m_indices = -1; out and out_scale rows no pair fills
+ * are not written.
+ */
+int oracle_permute_ex(const uint8_t *x, int64_t row_bytes, const uint32_t *x_scale,
+                      int scale_cols, int scale_col_major, int64_t scale_ld,
+                      const int64_t *topk_idx, int T, int k, int E, int e_begin, int e_end,
+                      const int32_t *expert_start_loc, int64_t capacity, uint8_t *out,
+                      uint32_t *out_scale, int32_t *m_indices, int32_t *output_index) {
+    if (T < 0 || k < 0 || E < 1 || row_bytes < 0 || capacity < 0) return ORC_ERR_INVALID_ARG;
+    if (e_begin < 0 || e_end > E || e_begin >= e_end) return ORC_ERR_INVALID_ARG;
+    if (scale_col_major && scale_ld < capacity) return ORC_ERR_INVALID_ARG;
+    int32_t fill_count[E];
+    for (int e = 0; e < E; ++e) fill_count[e] = 0;
+    for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;
+    const int64_t base = expert_start_loc[e_begin];
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t e = topk_idx[(int64_t)t * k + j];
+            if (e < -1 || e >= E) return ORC_ERR_INVALID_EXPERT;
+            if (e < e_begin || e >= e_end) {  /* no pick, or an expert of another view */
+                output_index[(int64_t)t * k + j] = -1;
+                continue;
+            }
+            int64_t s = (int64_t)expert_start_loc[e] - base + fill_count[e];
+            fill_count[e] += 1;
+            if (s < 0 || s >= capacity) return ORC_ERR_CAPACITY;
+            output_index[(int64_t)t * k + j] = (int32_t)s;
+            m_indices[s] = (int32_t)(e - e_begin);
+            memcpy(out + s * row_bytes, x + (int64_t)t * row_bytes, (size_t)row_bytes);
+            for (int c = 0; c < scale_cols; ++c) {
+                uint32_t v = x_scale[(int64_t)t * scale_cols + c];
+                if (scale_col_major) out_scale[(int64_t)c * scale_ld + s] = v;
+                else out_scale[s * scale_cols + c] = v;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/*
  * bf16 from a double, round to nearest, ties to even, written from the format's
  * definition (8 significant bits, fp32's exponent range, subnormal spacing
  * 2^-133): scale to the spacing of the value's binade, round the scaled value to

@@ -330,3 +330,109 @@ def check_combine_all(orc):
     check_combine_identity(orc)
     check_combine_one_hot(orc)
     check_combine_exact_sums(orc)
+
+
+# ----------------------------------------------------------------------------- views and scale layouts
+def check_hand_example_rank3(orc):
+    g = load_golden("hand_example_rank3.json")
+    topk = np.array(g["topk_idx"], np.int64)
+    T = topk.shape[0]
+    lay = orc.dispatch_layout(topk, g["E"], g["R"], g["N"])
+    start, _ = orc.scan_offsets(lay["tokens_per_expert"])
+    r = orc.permute_ex(token_id_rows(T), None, topk, g["E"], start, g["capacity"],
+                       expert_begin=g["expert_begin"], expert_end=g["expert_end"])
+    assert r["output_index"].tolist() == g["output_index"]
+    assert r["m_indices"].tolist() == g["m_indices"]
+    n = len(g["permuted_source_tokens"])
+    assert rows_to_token_ids(r["out"][:n]) == g["permuted_source_tokens"]
+
+
+def reference_view(topk, E, b, e_end, alignment=1, scale_words=None, capacity=None):
+    """Independent definition of one view: counts by Counter, offsets by numpy's
+    cumulative sum of the (padded) counts, slots by sorting the view's pairs by
+    (expert, token, slot); scale rows placed by numpy indexing."""
+    T, k = topk.shape
+    pairs = [(int(topk[t, j]), t, j) for t in range(T) for j in range(k) if topk[t, j] >= 0]
+    cnt = Counter(e for (e, _, _) in pairs)
+    counts = np.array([cnt.get(e, 0) for e in range(E)], np.int64)
+    padded = -(-counts // alignment) * alignment
+    start = np.concatenate([[0], np.cumsum(padded)[:-1]]).astype(np.int64)
+    base = start[b]
+    if capacity is None:
+        capacity = T * k
+    oi = -np.ones((T, k), np.int64)
+    mi = -np.ones(capacity, np.int64)
+    seen = Counter()
+    for (e, t, j) in sorted(p for p in pairs if b <= p[0] < e_end):
+        s = start[e] - base + seen[e]
+        seen[e] += 1
+        oi[t, j] = s
+        mi[s] = e - b
+    res = dict(output_index=oi, m_indices=mi, start=start)
+    if scale_words is not None:
+        C = scale_words.shape[1]
+        rm = np.zeros((capacity, C), np.uint32)
+        valid = oi >= 0
+        rows = oi[valid]
+        toks = np.nonzero(valid)[0]
+        rm[rows] = scale_words[toks]
+        res["scale_row_major"] = rm
+    return res
+
+
+def check_view_against_reference(orc, topk, E, b, e_end, alignment=1, col_major=False, seed=0):
+    T, k = topk.shape
+    cap = T * k if alignment == 1 else orc.aligned_capacity(T, k, E, alignment)
+    rng = np.random.default_rng(seed)
+    words = rng.integers(0, 2 ** 32, size=(T, 5), dtype=np.uint64).astype(np.uint32)
+    ref = reference_view(topk, E, b, e_end, alignment, words, cap)
+    lay = orc.dispatch_layout(topk, E, 1, 1)
+    if alignment == 1:
+        start, _ = orc.scan_offsets(lay["tokens_per_expert"])
+    else:
+        start, _ = orc.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
+    assert start.tolist() == ref["start"].tolist()
+    ld = cap + 12 if col_major else None
+    x = token_id_rows(T)
+    r = orc.permute_ex(x, words, topk, E, start, cap, expert_begin=b, expert_end=e_end,
+                       scale_col_major=col_major, scale_ld=ld)
+    assert r["output_index"].tolist() == ref["output_index"].tolist(), "output_index"
+    assert r["m_indices"].tolist() == ref["m_indices"].tolist(), "m_indices"
+    valid = ref["output_index"] >= 0
+    rows = ref["output_index"][valid]
+    assert rows_to_token_ids(r["out"][rows]) == np.nonzero(valid)[0].tolist(), "rows"
+    if col_major:
+        got = r["out_scale"][:, :cap].T          # [C, ld] column-major -> [cap, C]
+    else:
+        got = r["out_scale"]
+    assert np.array_equal(got[rows], ref["scale_row_major"][rows]), "scales"
+
+
+def check_views_tile_the_buffer(orc, topk, E, R, alignment=1):
+    """The per-rank views, placed at their region offsets, rebuild the whole buffer."""
+    T, k = topk.shape
+    cap = T * k if alignment == 1 else orc.aligned_capacity(T, k, E, alignment)
+    lay = orc.dispatch_layout(topk, E, R, 1)
+    if alignment == 1:
+        start, total = orc.scan_offsets(lay["tokens_per_expert"])
+    else:
+        start, total = orc.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
+    x = token_id_rows(T)
+    full = orc.permute(x, None, topk, E, start, cap)
+    epr = E // R
+    oi_all = -np.ones((T, k), np.int64)
+    for r in range(R):
+        b, e_end = r * epr, (r + 1) * epr
+        v = orc.permute_ex(x, None, topk, E, start, cap, expert_begin=b, expert_end=e_end)
+        base = int(start[b])
+        end = int(start[e_end]) if e_end < E else total
+        n = end - base
+        mi = v["m_indices"][:n]
+        want = full["m_indices"][base:end]
+        assert np.array_equal(np.where(mi >= 0, mi + b, -1), want)
+        assert np.all(v["m_indices"][n:] == -1)
+        sel = v["output_index"] >= 0
+        oi_all[sel] = v["output_index"][sel] + base
+        rows = v["output_index"][sel]
+        assert np.array_equal(v["out"][rows], full["out"][rows + base])
+    assert np.array_equal(oi_all, full["output_index"])

@@ -10,7 +10,8 @@ import pytest
 
 import oracle as oracle_pkg
 from oracle_pins import (check_bf16_rounding, check_bruteforce, check_combine_all,
-                         check_hand_example, check_hand_example_aligned, check_invariants)
+                         check_hand_example, check_hand_example_aligned,
+                         check_hand_example_rank3, check_invariants, check_view_against_reference)
 
 SRC = os.path.join(os.path.dirname(oracle_pkg.__file__), "epd_oracle.c")
 
@@ -20,13 +21,23 @@ MUTANTS = {
     "interleaved_ranks": ("return (int)(e / (E / R));", "return (int)(e % R);"),
     "interleaved_nodes": ("return r / (R / N);", "return r % N;"),
     "pairs_not_tokens": ("in_rank = 1;", "in_rank += 1;"),
-    "dropped_fill_increment": ("fill_count[e] += 1;", ""),
+    "dropped_fill_increment": ("fill_count[e] += 1;", "", 0),
+    "dropped_fill_increment_view": ("fill_count[e] += 1;", "", 1),
     "m_indices_wrong_operand": ("m_indices[s] = (int32_t)e;", "m_indices[s] = (int32_t)t;"),
-    "unfilled_rows_not_cleared": ("for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;", ""),
+    "unfilled_rows_not_cleared": ("for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;", "",
+                                  0),
     "first_row_not_cleared": ("for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;",
-                              "for (int64_t s = 1; s < capacity; ++s) m_indices[s] = -1;"),
+                              "for (int64_t s = 1; s < capacity; ++s) m_indices[s] = -1;", 0),
+    "unfilled_rows_not_cleared_view": (
+        "for (int64_t s = 0; s < capacity; ++s) m_indices[s] = -1;", "", 1),
     "alignment_rounds_down": ("run += (c + alignment - 1) / alignment * alignment;",
                               "run += c / alignment * alignment;"),
+    "view_global_ids": ("m_indices[s] = (int32_t)(e - e_begin);", "m_indices[s] = (int32_t)e;"),
+    "view_base_not_subtracted": ("int64_t s = (int64_t)expert_start_loc[e] - base + fill_count[e];",
+                                 "int64_t s = (int64_t)expert_start_loc[e] + fill_count[e];"),
+    "scale_col_major_swapped": ("if (scale_col_major) out_scale[(int64_t)c * scale_ld + s] = v;",
+                                "if (scale_col_major) out_scale[s * scale_ld + c] = v;"),
+    "view_range_off_by_one": ("if (e < e_begin || e >= e_end) {", "if (e < e_begin || e > e_end) {"),
     "alignment_ignored": ("run += (c + alignment - 1) / alignment * alignment;", "run += c;"),
     "weight_wrong_index": ("acc += (double)topk_weights[(int64_t)t * k + j] *",
                            "acc += (double)topk_weights[(int64_t)t * k] *"),
@@ -39,13 +50,27 @@ MUTANTS = {
 }
 
 
+def _mutate(src, before, after, which):
+    """Replace occurrence `which` (0-based) of `before`; `which` None needs it unique."""
+    n = src.count(before)
+    if which is None:
+        assert n == 1, f"mutation site not unique ({n})"
+        return src.replace(before, after)
+    assert n > which, f"mutation site {which} missing ({n})"
+    i = -1
+    for _ in range(which + 1):
+        i = src.index(before, i + 1)
+    return src[:i] + after + src[i + len(before):]
+
+
 def _load_mutant(tmp_path, name):
-    before, after = MUTANTS[name]
+    spec = MUTANTS[name]
+    before, after = spec[0], spec[1]
+    which = spec[2] if len(spec) > 2 else None
     src = open(SRC).read()
-    assert src.count(before) == 1, f"mutation site for {name} not unique"
     d = tmp_path / name
     (d / "_build").mkdir(parents=True)
-    (d / "epd_oracle.c").write_text(src.replace(before, after))
+    (d / "epd_oracle.c").write_text(_mutate(src, before, after, which))
     shutil.copy(oracle_pkg.__file__, d / "__init__.py")
     spec = importlib.util.spec_from_file_location(f"oracle_mutant_{name}", d / "__init__.py")
     mod = importlib.util.module_from_spec(spec)
@@ -57,6 +82,11 @@ def _run_pins(orc):
     check_hand_example(orc)
     check_hand_example_aligned(orc)
     check_bruteforce(orc, 2, 2, 4, 2, 1, limit=2000, alignment=4)
+    check_hand_example_rank3(orc)
+    for flat in [(0, 3, 1, 2, -1, 3), (3, 3, 2, 1, 0, 0), (1, 2, 2, 3, 3, -1)]:
+        t = np.array(flat, np.int64).reshape(3, 2)
+        check_view_against_reference(orc, t, 4, 1, 4, 1, True)
+        check_view_against_reference(orc, t, 4, 2, 3, 1, False)
     check_bruteforce(orc, 3, 2, 4, 2, 1, limit=3000)
     check_bruteforce(orc, 2, 2, 4, 4, 2, limit=3000)
     rng = np.random.default_rng(0)

@@ -144,3 +144,37 @@ def test_alignment_one_is_the_plain_scan():
     a, ta = oracle.scan_offsets_aligned(cnt, 1)
     b, tb = oracle.scan_offsets(cnt)
     assert a.tolist() == b.tolist() and ta == tb
+
+
+# ----------------------------------------------------------------------------- views and scale layouts
+from oracle_pins import (check_hand_example_rank3, check_view_against_reference,  # noqa: E402
+                         check_views_tile_the_buffer)
+
+
+def test_hand_example_rank3():
+    """The worked routing seen from simulated rank 3 (experts 6 and 7, local ids 0, 1)."""
+    check_hand_example_rank3(oracle)
+
+
+@pytest.mark.parametrize("b,e_end,alignment,col_major", [
+    (0, 4, 1, False), (1, 3, 1, True), (2, 4, 2, False), (0, 2, 4, True), (3, 4, 1, True),
+])
+def test_views_bruteforce(b, e_end, alignment, col_major):
+    import itertools
+    for n, flat in enumerate(itertools.product(range(-1, 4), repeat=6)):
+        if n % 3:
+            continue
+        topk = np.array(flat, np.int64).reshape(3, 2)
+        check_view_against_reference(oracle, topk, 4, b, e_end, alignment, col_major, seed=n)
+
+
+@pytest.mark.parametrize("alignment", [1, 8, 128])
+def test_views_tile_the_buffer(alignment):
+    c = workloads.make_case("dsv3_fp8", T=200)
+    check_views_tile_the_buffer(oracle, c.topk_idx.numpy(), c.E, c.R, alignment)
+
+
+def test_views_on_workload_shapes():
+    c = workloads.make_case("skew_bf16", T=300, experts="identity")
+    for b, e in [(0, 8), (64, 72), (248, 256)]:
+        check_view_against_reference(oracle, c.topk_idx.numpy(), c.E, b, e, 1, True)

@@ -61,7 +61,7 @@ class Case:
     topk_idx: torch.Tensor           # [T, k] int64, -1 = no selection
     topk_weights: torch.Tensor       # [T, k] float32 (0 where topk_idx == -1)
     x: torch.Tensor                  # [T, H] bfloat16 or float8_e4m3fn
-    x_scale: Optional[torch.Tensor]  # [T, H/128] float32 (fp8 only)
+    x_scale: Optional[torch.Tensor]  # [T, H/128] float32, or [T, ceil(H/512)] int32 UE8M0 (fp8)
     expert_out: Optional[torch.Tensor]  # [T*k, H] bfloat16, or None = identity experts
     meta: dict = field(default_factory=dict)
 
@@ -136,6 +136,29 @@ def quantize_fp8_per128(x: torch.Tensor):
     return q.reshape(T, H), scale.float().contiguous()
 
 
+def quantize_fp8_per128_ue8m0(x: torch.Tensor):
+    """Per-(row, 128-column block) e4m3 quantisation with power-of-two scales, the
+    form whose scales pack as UE8M0 bytes (an 8-bit biased exponent, no mantissa):
+    scale = 2^ceil(log2(amax / 448)) (1 where the block is all zero), q = e4m3(x /
+    scale). Returns (q [T, H] e4m3, words [T, ceil(H/512)] int32), four exponent
+    bytes per word, block 4g in the lowest byte, missing blocks padded with 127
+    (scale 1)."""
+    T, H = x.shape
+    C = H // 128
+    blocks = x.reshape(T, C, 128).double()
+    amax = blocks.abs().amax(dim=2)
+    expo = torch.where(amax > 0, torch.ceil(torch.log2(amax / FP8_MAX)), torch.zeros_like(amax))
+    scale = torch.pow(2.0, expo)
+    q = (blocks / scale.unsqueeze(2)).clamp_(-FP8_MAX, FP8_MAX).float().to(torch.float8_e4m3fn)
+    G = (C + 3) // 4
+    byte = torch.full((T, 4 * G), 127, dtype=torch.int64)
+    byte[:, :C] = (expo + 127).to(torch.int64)
+    b = byte.reshape(T, G, 4)
+    words = (b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24))
+    words = torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
+    return q.reshape(T, H), words.contiguous()
+
+
 def _randn_bf16(g, rows, cols, chunk_rows=8192):
     out = torch.empty(rows, cols, dtype=torch.bfloat16)
     for r0 in range(0, rows, chunk_rows):
@@ -144,18 +167,20 @@ def _randn_bf16(g, rows, cols, chunk_rows=8192):
     return out
 
 
-def make_rows(g, T, H, dtype):
+def make_rows(g, T, H, dtype, scales="f32"):
     if dtype == "bf16":
         return _randn_bf16(g, T, H), None
     if dtype == "fp8":
         if H % 128:
             raise ValueError("fp8 rows need H % 128 == 0")
+        if scales == "ue8m0":
+            return quantize_fp8_per128_ue8m0(torch.randn(T, H, generator=g))
         return quantize_fp8_per128(torch.randn(T, H, generator=g))
     raise ValueError(dtype)
 
 
 def make_case(name: str = "tiny", seed: Optional[int] = None, T: Optional[int] = None,
-              experts: Optional[str] = None) -> Case:
+              experts: Optional[str] = None, scales: str = "f32") -> Case:
     """Build one named workload (see CONFIGS). ``T`` overrides the token count
     (smaller instances of the same routing shape); ``experts`` overrides the
     expert-output mode ("identity" or "random")."""
@@ -170,11 +195,14 @@ def make_case(name: str = "tiny", seed: Optional[int] = None, T: Optional[int] =
                             N=cfg["N"], dtype=cfg["dtype"], seed=seed,
                             routing=cfg["routing"], p_invalid=cfg.get("p_invalid", 0.0),
                             experts=cfg["experts"], zipf_s=cfg.get("zipf_s", 1.2),
-                            zero_experts=cfg.get("zero_experts", 20), name=name)
+                            zero_experts=cfg.get("zero_experts", 20), name=name, scales=scales)
 
 
 def make_random_case(T, H, k, E, R, N, dtype="bf16", seed=0, routing="uniform", p_invalid=0.0,
-                     experts="random", zipf_s=1.2, zero_experts=20, name="random") -> Case:
+                     experts="random", zipf_s=1.2, zero_experts=20, name="random",
+                     scales="f32") -> Case:
+    """scales: "f32" (one fp32 scale per 128 columns) or "ue8m0" (power-of-two scales
+    packed as exponent bytes, four per int32 word; x_scale is then int32)."""
     g = _gen(seed)
     meta = {}
     if T == 0 or k == 0:
@@ -197,7 +225,7 @@ def make_random_case(T, H, k, E, R, N, dtype="bf16", seed=0, routing="uniform", 
         w = torch.zeros(T, k, dtype=torch.float32)
     else:
         raise ValueError(routing)
-    x, x_scale = make_rows(g, T, H, dtype)
+    x, x_scale = make_rows(g, T, H, dtype, scales)
     if experts == "random":
         eo = _randn_bf16(g, T * k, H)
     elif experts == "identity":
