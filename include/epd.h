@@ -193,6 +193,48 @@ EPD_API epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float *x
                         int32_t *output_index, int32_t *status, epd_stream_t stream);
 
 /*
+ * Output options of ep_permute_ex.
+ *   expert_begin, expert_end: the view -- only pairs whose expert is in
+ *     [expert_begin, expert_end) are placed (0 and num_experts for all
+ *     experts). A simulated rank r of R holds [r*E/R, (r+1)*E/R). Rows are
+ *     relative to the view's first region: a pair's row is
+ *     expert_start_loc[e] - expert_start_loc[expert_begin] + its rank inside e,
+ *     m_indices holds the local id e - expert_begin, and pairs outside the view
+ *     get output_index = -1.
+ *   scale_cols: 32-bit scale words per token (H/128 fp32 scales, or
+ *     ceil(H/512) words of four packed UE8M0 exponent bytes); 0 for none.
+ *   scale_col_major: 0 stores word c of row s at out_scale[s * scale_cols + c];
+ *     1 stores it at out_scale[c * scale_ld + s] (column-major, the layout a
+ *     TMA-fed grouped GEMM reads), scale_ld >= capacity_rows.
+ */
+typedef struct {
+    int expert_begin;
+    int expert_end;
+    int scale_cols;
+    int scale_col_major;
+    int64_t scale_ld;
+} epd_permute_view_t;
+
+/*
+ * Step 3 with output options: a per-rank view ([P1] 3.1.2 and 7: after dispatch
+ * a rank's topk ids are local, rank_expert_offset maps them; [P1] 3.3:
+ * deepgemm_moe_permute over local_num_experts) and scale layouts ([P1] 2.2:
+ * UE8M0 scales as an int tensor [ceil(H/512), M] viewed transposed; [P3]
+ * low_latency_dispatch docstring: scales column-major for TMA). Rows are any
+ * row_bytes (a multiple of 16) copied verbatim; `view` is a host pointer.
+ * capacity_rows must hold the view's regions (a slot outside sets
+ * EPD_ERR_CAPACITY). Otherwise as ep_permute, which is this call with the whole
+ * expert range and row-major fp32 scales.
+ */
+EPD_API epd_status_t ep_permute_ex(const void *x, int64_t row_bytes, const void *x_scale,
+                                   const int64_t *topk_idx, int num_tokens, int num_topk,
+                                   int num_experts, const int32_t *expert_start_loc,
+                                   const void *workspace, int64_t capacity_rows,
+                                   const epd_permute_view_t *view, void *out, void *out_scale,
+                                   int32_t *m_indices, int32_t *output_index, int32_t *status,
+                                   epd_stream_t stream);
+
+/*
  * Step 4 -- unpermute (combine). [P3] "Dispatch" (combine is the reverse of
  * dispatch; topk_weights are fp32 [T, k]):
  *   y[t, h] = bf16( sum over j with output_index[t, j] != -1, in j order, of

@@ -142,3 +142,23 @@ def test_binding_fails_loudly_without_library(tmp_path):
             _binding.load_library(missing)
     finally:
         _binding._lib = saved
+
+
+def test_permute_ex_rejects_bad_views(lib):
+    E = _binding.EPD_ERR_INVALID_ARG
+    f = lib.ep_permute_ex
+
+    def call(view, row_bytes=64, cap=8, xs=NULL, outs=NULL):
+        return f(FAKE, row_bytes, xs, FAKE, 4, 2, 8, FAKE, FAKE, cap, ctypes.byref(view), FAKE,
+                 outs, FAKE, FAKE, FAKE, NULL)
+    V = _binding.PermuteView
+    assert f(FAKE, 64, NULL, FAKE, 4, 2, 8, FAKE, FAKE, 8, None, FAKE, NULL, FAKE, FAKE, FAKE,
+             NULL) == E                                           # no view
+    assert call(V(0, 9, 0, 0, 0)) == E                           # past num_experts
+    assert call(V(4, 4, 0, 0, 0)) == E                           # empty range
+    assert call(V(-1, 4, 0, 0, 0)) == E
+    assert call(V(0, 8, 0, 2, 0)) == E                           # unknown scale layout
+    assert call(V(0, 8, 3, 1, 4), xs=FAKE, outs=FAKE) == E       # ld below capacity
+    assert call(V(0, 8, 3, 0, 0)) == E                           # scales without pointers
+    assert call(V(0, 8, 0, 0, 0), row_bytes=60) == E             # rows not 16-byte multiples
+    assert call(V(0, 8, 0, 0, 0), cap=-1) == E

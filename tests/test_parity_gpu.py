@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import unpermute_ep_dispatch_gb300 as epd
-from epd_paths import GpuPath, bits16, compare, oracle_path
+from epd_paths import GpuPath, bits16, compare, oracle_path, row_bytes
 from unpermute_ep_dispatch_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -289,3 +289,64 @@ def test_aligned_edges(T, p_invalid):
                                       routing="repeats", p_invalid=p_invalid, experts="random")
     got, want, _ = run_both(case, alignment=64)
     compare(got, want)
+
+
+# ----------------------------------------------------------------------------- views and scale layouts
+def _words(t):
+    return t.detach().cpu().contiguous().view(torch.int32).numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("scales", ["f32", "ue8m0"])
+@pytest.mark.parametrize("col_major", [False, True])
+@pytest.mark.parametrize("alignment", [1, 128])
+def test_permute_views_and_scale_layouts(scales, col_major, alignment):
+    import oracle
+    case = workloads.make_case("dsv3_fp8", T=2048, scales=scales)
+    g = GpuPath(case, alignment=alignment)
+    g.layout()
+    g.scan()
+    torch.cuda.synchronize()
+    lay = oracle.dispatch_layout(case.topk_idx.numpy(), case.E, case.R, case.N)
+    if alignment == 1:
+        ostart, _ = oracle.scan_offsets(lay["tokens_per_expert"])
+    else:
+        ostart, _ = oracle.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
+    assert np.array_equal(g.start.cpu().numpy(), ostart)
+    xs = case.x_scale.to(g.dev)
+    xrows = row_bytes(case.x)
+    for r in (0, 13, 31):
+        b, e = r * 8, r * 8 + 8
+        cap = 2048 * 8 // 4 + 8 * alignment         # a rank's rows stay far below this here
+        ld = cap + 4 if col_major else None
+        out, osc, mi, oi = epd.ep_permute_ex(g.x, xs, g.topk, case.E, g.start, g.ws, g.status,
+                                             capacity_rows=cap, expert_begin=b, expert_end=e,
+                                             scale_col_major=col_major, scale_ld=ld)
+        torch.cuda.synchronize()
+        assert int(g.status.item()) == 0
+        want = oracle.permute_ex(xrows, _words(case.x_scale), case.topk_idx.numpy(), case.E,
+                                 ostart, cap, expert_begin=b, expert_end=e,
+                                 scale_col_major=col_major, scale_ld=ld)
+        got_oi = oi.cpu().numpy()
+        assert np.array_equal(got_oi, want["output_index"])
+        assert np.array_equal(mi.cpu().numpy(), want["m_indices"])
+        rows = got_oi[got_oi >= 0]
+        assert np.array_equal(row_bytes(out)[rows], want["out"][rows])
+        gs = _words(osc)
+        if col_major:
+            assert np.array_equal(gs[:, rows], want["out_scale"][:, rows])
+        else:
+            assert np.array_equal(gs[rows], want["out_scale"][rows])
+
+
+def test_permute_ex_whole_range_equals_permute():
+    case = workloads.make_case("prefill_bf16", T=1500)
+    g = GpuPath(case)
+    g.step()
+    ref = g.results()
+    out, _, mi, oi = epd.ep_permute_ex(g.x, None, g.topk, case.E, g.start, g.ws, g.status,
+                                       capacity_rows=g.cap)
+    torch.cuda.synchronize()
+    assert np.array_equal(oi.cpu().numpy(), ref["output_index"])
+    assert np.array_equal(mi.cpu().numpy(), ref["m_indices"])
+    rows = ref["output_index"][ref["output_index"] >= 0]
+    assert np.array_equal(row_bytes(out)[rows], ref["out"][rows])

@@ -31,6 +31,13 @@ EPD_FP8_E4M3 = 1
 EPD_MAX_EXPERTS = 4096
 EPD_MAX_TOPK = 64
 
+class PermuteView(ctypes.Structure):
+    """epd_permute_view_t."""
+    _fields_ = [("expert_begin", ctypes.c_int), ("expert_end", ctypes.c_int),
+                ("scale_cols", ctypes.c_int), ("scale_col_major", ctypes.c_int),
+                ("scale_ld", ctypes.c_int64)]
+
+
 # name -> (restype, argtypes); mirrors include/epd.h
 _P, _I, _I64, _U32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
                            ctypes.c_size_t)
@@ -44,6 +51,8 @@ SIGNATURES = {
     "ep_scan_offsets": (_I, [_P, _I, _P, _P, _P, _P]),
     "ep_scan_offsets_aligned": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "ep_permute": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
+    "ep_permute_ex": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _I64, ctypes.POINTER(PermuteView),
+                           _P, _P, _P, _P, _P, _P]),
     "ep_unpermute": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _P]),
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "epd_test_layout_stalled_tile": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
@@ -275,6 +284,56 @@ def ep_permute(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: torch
                                    _ptr(out), _ptr(out_scale), _ptr(m_indices),
                                    _ptr(output_index), _ptr(status), _stream(stream, dev))
     _check(rc, "ep_permute")
+    return out, out_scale, m_indices, output_index
+
+
+def ep_permute_ex(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: torch.Tensor,
+                  num_experts: int, expert_start_loc: torch.Tensor, workspace: torch.Tensor,
+                  status: torch.Tensor, capacity_rows: Optional[int] = None,
+                  expert_begin: int = 0, expert_end: Optional[int] = None,
+                  scale_col_major: bool = False, scale_ld: Optional[int] = None, out=None,
+                  out_scale=None, m_indices=None, output_index=None, stream=None):
+    """Step 3 with a per-rank view [expert_begin, expert_end) and a scale layout.
+    x: [T, *] rows of any dtype (row bytes a multiple of 16); x_scale: [T, C]
+    float32 (fp32 scales) or int32 (UE8M0-packed words), or None. Returns (out
+    [M, *], out_scale ([M, C] row-major or [C, scale_ld] column-major) or None,
+    m_indices [M] (local expert ids), output_index [T, k] (rows of the view))."""
+    _want(x, "x", x.dtype)
+    dev = x.device
+    T = x.shape[0]
+    row_bytes = int(torch.Size(x.shape[1:]).numel()) * x.element_size()
+    _want(topk_idx, "topk_idx", torch.int64, device=dev)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, k] with the T of x")
+    k = topk_idx.shape[1]
+    E = int(num_experts)
+    e_end = E if expert_end is None else int(expert_end)
+    M = T * k if capacity_rows is None else int(capacity_rows)
+    _want(expert_start_loc, "expert_start_loc", torch.int32, (E,), dev)
+    _want(workspace, "workspace", torch.uint8, device=dev)
+    _want(status, "status", torch.int32, (1,), dev)
+    out = _out(out, "out", x.dtype, (M, *x.shape[1:]), dev)
+    C = 0
+    if x_scale is not None:
+        if x_scale.dtype not in (torch.float32, torch.int32) or x_scale.dim() != 2:
+            raise ValueError("x_scale must be [T, C] float32 or int32")
+        _want(x_scale, "x_scale", x_scale.dtype, (T, x_scale.shape[1]), dev)
+        C = x_scale.shape[1]
+        ld = M if scale_ld is None else int(scale_ld)
+        shape = (C, ld) if scale_col_major else (M, C)
+        out_scale = _out(out_scale, "out_scale", x_scale.dtype, shape, dev)
+    else:
+        ld = 0
+        out_scale = None
+    m_indices = _out(m_indices, "m_indices", torch.int32, (M,), dev)
+    output_index = _out(output_index, "output_index", torch.int32, (T, k), dev)
+    view = PermuteView(int(expert_begin), e_end, C, int(bool(scale_col_major)), ld)
+    rc = load_library().ep_permute_ex(_ptr(x), row_bytes, _ptr(x_scale), _ptr(topk_idx), T, k, E,
+                                      _ptr(expert_start_loc), _ptr(workspace), M,
+                                      ctypes.byref(view), _ptr(out), _ptr(out_scale),
+                                      _ptr(m_indices), _ptr(output_index), _ptr(status),
+                                      _stream(stream, dev))
+    _check(rc, "ep_permute_ex")
     return out, out_scale, m_indices, output_index
 
 

@@ -26,8 +26,11 @@ constexpr int kUnitVecs = 64;  // 16-byte vectors per work unit (1 KiB of a row)
 struct PermuteArgs {
     const uint8_t *x;
     int64_t row_bytes;
-    const float *x_scale;
+    const uint32_t *x_scale;  // 32-bit scale words (fp32 scales or packed UE8M0 bytes)
     int scale_cols;
+    int scale_col_major;      // 0: out_scale[s * scale_cols + c]; 1: out_scale[c * scale_ld + s]
+    int64_t scale_ld;
+    int e_begin, e_end;       // experts of the view; rows are relative to start[e_begin]
     const int64_t *topk;
     int T, k, E;
     const int32_t *start;
@@ -36,7 +39,7 @@ struct PermuteArgs {
     const WsHeader *hdr;
     int64_t capacity;
     uint8_t *out;
-    float *out_scale;
+    uint32_t *out_scale;
     int32_t *m_indices;
     int32_t *output_index;
     int32_t *status;
@@ -47,17 +50,24 @@ struct PermuteArgs {
 // empty regions), and holds that expert when it is among the region's first
 // count rows, else -1 (alignment padding, or rows after the last region). Works
 // for plain and aligned offsets alike; coalesced, one binary search per row.
-__device__ __forceinline__ void fill_m_indices(const PermuteArgs &a, int64_t first, int64_t stride) {
+__device__ __forceinline__ void fill_m_indices(const PermuteArgs &a, int64_t base, int64_t first,
+                                               int64_t stride) {
     for (int64_t s = first; s < a.capacity; s += stride) {
-        int lo = 0, hi = a.E - 1;
-        while (lo < hi) {  // last e with start[e] <= s
+        const int64_t g = s + base;  // row in the offsets' coordinates
+        int lo = a.e_begin, hi = a.e_end - 1;
+        while (lo < hi) {  // last e of the view with start[e] <= g
             const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)__ldg(a.start + mid) <= s) lo = mid;
+            if ((int64_t)__ldg(a.start + mid) <= g) lo = mid;
             else hi = mid - 1;
         }
         const int64_t st = __ldg(a.start + lo);
-        a.m_indices[s] = (s >= st && s < st + __ldg(a.counts + lo)) ? lo : -1;
+        a.m_indices[s] = (g >= st && g < st + __ldg(a.counts + lo)) ? lo - a.e_begin : -1;
     }
+}
+
+// Row of the scale word c of buffer row s.
+__device__ __forceinline__ int64_t scale_index(const PermuteArgs &a, int64_t s, int c) {
+    return a.scale_col_major ? (int64_t)c * a.scale_ld + s : s * a.scale_cols + c;
 }
 
 __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
@@ -72,6 +82,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     }
     __syncthreads();
     if (!s_ok) return;
+    const int64_t base = a.start[a.e_begin];  // first row of the view in offset coordinates
 
     const int64_t row_vecs = a.row_bytes >> 4;
     const int upt = (int)((row_vecs + kUnitVecs - 1) / kUnitVecs);  // units per token
@@ -93,8 +104,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
                 const int64_t idx = (int64_t)t * a.k + j;
                 const int64_t e = a.topk[idx];
                 int s = -1;
-                if (e >= 0 && e < a.E) {
-                    const int64_t sl = (int64_t)a.start[e] + a.pair_rank[idx];
+                if (e >= a.e_begin && e < a.e_end) {
+                    const int64_t sl = (int64_t)a.start[e] - base + a.pair_rank[idx];
                     if (sl >= 0 && sl < a.capacity) s = (int)sl;
                     else if (ch == 0) report(a.status, EPD_ERR_CAPACITY);
                 }
@@ -120,10 +131,10 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
         }
         if (ch == 0) {  // fp8 scale row travels with chunk 0
             for (int c = lane; c < a.scale_cols; c += 32) {
-                const float sv = a.x_scale[(int64_t)t * a.scale_cols + c];
+                const uint32_t sv = a.x_scale[(int64_t)t * a.scale_cols + c];
                 for (int j = 0; j < a.k; ++j) {
                     const int s = s_slot[warp][j];
-                    if (s >= 0) a.out_scale[(int64_t)s * a.scale_cols + c] = sv;
+                    if (s >= 0) a.out_scale[scale_index(a, s, c)] = sv;
                 }
             }
         }
@@ -132,7 +143,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    fill_m_indices(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    fill_m_indices(a, base, (int64_t)blockIdx.x * kThreads + threadIdx.x,
+                   (int64_t)gridDim.x * kThreads);
 }
 
 // ----------------------------------------------------------------------------- bulk-copy variant
@@ -190,6 +202,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     }
     __syncthreads();
     if (!s_ok) return;
+    const int64_t base = a.start[a.e_begin];  // first row of the view in offset coordinates
 
     const int B = tma_batch_tokens(a.k);
     const int S = L.stages;
@@ -206,8 +219,8 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
             const int64_t idx = (int64_t)(b0 + tl) * a.k + (i - tl * a.k);
             const int64_t e = a.topk[idx];
             int s = -1;
-            if (e >= 0 && e < a.E) {
-                const int64_t sl = (int64_t)a.start[e] + a.pair_rank[idx];
+            if (e >= a.e_begin && e < a.e_end) {
+                const int64_t sl = (int64_t)a.start[e] - base + a.pair_rank[idx];
                 if (sl >= 0 && sl < a.capacity) {
                     s = (int)sl;
                 } else {
@@ -268,10 +281,10 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
             if (t2 >= 0) {
                 for (int i = t2; i < nb * a.scale_cols; i += nthreads) {
                     const int tl = i / a.scale_cols, c = i - tl * a.scale_cols;
-                    const float sv = a.x_scale[(int64_t)(b0 + tl) * a.scale_cols + c];
+                    const uint32_t sv = a.x_scale[(int64_t)(b0 + tl) * a.scale_cols + c];
                     for (int j = 0; j < a.k; ++j) {
                         const int sl = s_slot[tl * a.k + j];
-                        if (sl >= 0) a.out_scale[(int64_t)sl * a.scale_cols + c] = sv;
+                        if (sl >= 0) a.out_scale[scale_index(a, sl, c)] = sv;
                     }
                 }
             }
@@ -284,72 +297,19 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    fill_m_indices(a, (int64_t)blockIdx.x * kTmaThreads + tid, (int64_t)gridDim.x * kTmaThreads);
+    fill_m_indices(a, base, (int64_t)blockIdx.x * kTmaThreads + tid,
+                   (int64_t)gridDim.x * kTmaThreads);
 }
 
 }  // namespace
 }  // namespace epd
 
-extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float *x_scale,
-                                   const int64_t *topk_idx, int num_tokens, int num_topk,
-                                   int hidden, int num_experts, const int32_t *expert_start_loc,
-                                   const void *workspace, int64_t capacity_rows, void *out,
-                                   float *out_scale, int32_t *m_indices, int32_t *output_index,
-                                   int32_t *status, epd_stream_t stream) {
-    using namespace epd;
-    const int T = num_tokens, k = num_topk, H = hidden, E = num_experts;
-    if (T < 0 || k < 0 || k > EPD_MAX_TOPK || E < 1 || E > EPD_MAX_EXPERTS || H <= 0)
-        return EPD_ERR_INVALID_ARG;
-    if ((int64_t)T * k > INT32_MAX) return EPD_ERR_INVALID_ARG;
-    if (capacity_rows < (int64_t)T * k || capacity_rows > INT32_MAX) return EPD_ERR_INVALID_ARG;
-    int64_t row_bytes;
-    int scale_cols;
-    if (dtype == EPD_BF16) {
-        if (H % 8 != 0 || x_scale != nullptr || out_scale != nullptr) return EPD_ERR_INVALID_ARG;
-        row_bytes = 2 * (int64_t)H;
-        scale_cols = 0;
-    } else if (dtype == EPD_FP8_E4M3) {
-        if (H % 128 != 0) return EPD_ERR_INVALID_ARG;
-        if (((int64_t)T * k > 0 && x_scale == nullptr) || (capacity_rows > 0 && out_scale == nullptr))
-            return EPD_ERR_INVALID_ARG;
-        if (!aligned4(x_scale) || !aligned4(out_scale)) return EPD_ERR_INVALID_ARG;
-        row_bytes = H;
-        scale_cols = H / 128;
-    } else {
-        return EPD_ERR_INVALID_ARG;
-    }
-    if (!expert_start_loc || !workspace || !status) return EPD_ERR_INVALID_ARG;
-    if (capacity_rows > 0 && !m_indices) return EPD_ERR_INVALID_ARG;
-    if ((int64_t)T * k > 0 && (!output_index || !topk_idx || !x || !out)) return EPD_ERR_INVALID_ARG;
-    if ((x && !aligned16(x)) || (out && !aligned16(out)) || (topk_idx && !aligned8(topk_idx)) ||
-        !aligned4(expert_start_loc) || !aligned16(workspace) || !aligned4(m_indices) ||
-        !aligned4(output_index) || !aligned4(status))
-        return EPD_ERR_INVALID_ARG;
+namespace epd {
+namespace {
 
-    const char *ws = static_cast<const char *>(workspace);
-    PermuteArgs a;
-    a.x = static_cast<const uint8_t *>(x);
-    a.row_bytes = row_bytes;
-    a.x_scale = x_scale;
-    a.scale_cols = scale_cols;
-    a.topk = topk_idx;
-    a.T = T;
-    a.k = k;
-    a.E = E;
-    a.start = expert_start_loc;
-    a.pair_rank = reinterpret_cast<const int32_t *>(ws + ws_pair_rank_off());
-    a.counts = reinterpret_cast<const int32_t *>(ws + ws_counts_off(T, k));
-    a.hdr = reinterpret_cast<const WsHeader *>(ws);
-    a.capacity = capacity_rows;
-    a.out = static_cast<uint8_t *>(out);
-    a.out_scale = out_scale;
-    a.m_indices = m_indices;
-    a.output_index = output_index;
-    a.status = status;
-
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+epd_status_t permute_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs) {
     // bulk-copy kernel when at least two row stages fit in shared memory
-    const TmaSmem L = tma_smem(row_bytes, k);
+    const TmaSmem L = tma_smem(a.row_bytes, k);
     if (L.stages >= 2) {
         static size_t opted = 0;
         if (L.total > opted) {
@@ -368,15 +328,131 @@ extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float
         }
         if (L.total <= opted) {
             // three blocks' worth of token runs per SM (measured best on GB300)
-            const int grid = (int)(T < 3 * sm_count() ? (T < 1 ? 1 : T) : 3 * sm_count());
+            const int64_t full = 3 * (int64_t)sm_count();
+            const int grid = (int)(T < full ? (T < 1 ? 1 : T) : full);
             return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
         }
     }
     static int resident = 0;
     if (resident == 0) resident = blocks_per_sm(permute_kernel, kThreads, 0);
-    const int64_t units = (int64_t)T * ((row_bytes / 16 + kUnitVecs - 1) / kUnitVecs);
+    const int64_t units = T * ((a.row_bytes / 16 + kUnitVecs - 1) / kUnitVecs);
     const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = (int64_t)sm_count() * resident;
     const int grid = (int)(want < 1 ? 1 : (want < full ? want : full));
     return launch_pdl(permute_kernel, grid, kThreads, 0, cs, a);
+}
+
+// Checks shared by both entry points; fills the common fields of `a`.
+epd_status_t permute_common(PermuteArgs &a, const void *x, int64_t row_bytes,
+                            const int64_t *topk_idx, int T, int k, int E,
+                            const int32_t *expert_start_loc, const void *workspace,
+                            int64_t capacity_rows, void *out, int32_t *m_indices,
+                            int32_t *output_index, int32_t *status) {
+    if (T < 0 || k < 0 || k > EPD_MAX_TOPK || E < 1 || E > EPD_MAX_EXPERTS) return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > INT32_MAX) return EPD_ERR_INVALID_ARG;
+    if (row_bytes <= 0 || row_bytes % 16 != 0) return EPD_ERR_INVALID_ARG;
+    if (capacity_rows < 0 || capacity_rows > INT32_MAX) return EPD_ERR_INVALID_ARG;
+    if (!expert_start_loc || !workspace || !status) return EPD_ERR_INVALID_ARG;
+    if (capacity_rows > 0 && !m_indices) return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > 0 && (!output_index || !topk_idx || !x || !out)) return EPD_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (out && !aligned16(out)) || (topk_idx && !aligned8(topk_idx)) ||
+        !aligned4(expert_start_loc) || !aligned16(workspace) || !aligned4(m_indices) ||
+        !aligned4(output_index) || !aligned4(status))
+        return EPD_ERR_INVALID_ARG;
+    const char *ws = static_cast<const char *>(workspace);
+    a.x = static_cast<const uint8_t *>(x);
+    a.row_bytes = row_bytes;
+    a.topk = topk_idx;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.start = expert_start_loc;
+    a.pair_rank = reinterpret_cast<const int32_t *>(ws + ws_pair_rank_off());
+    a.counts = reinterpret_cast<const int32_t *>(ws + ws_counts_off(T, k));
+    a.hdr = reinterpret_cast<const WsHeader *>(ws);
+    a.capacity = capacity_rows;
+    a.out = static_cast<uint8_t *>(out);
+    a.m_indices = m_indices;
+    a.output_index = output_index;
+    a.status = status;
+    return EPD_OK;
+}
+
+}  // namespace
+}  // namespace epd
+
+extern "C" epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float *x_scale,
+                                   const int64_t *topk_idx, int num_tokens, int num_topk,
+                                   int hidden, int num_experts, const int32_t *expert_start_loc,
+                                   const void *workspace, int64_t capacity_rows, void *out,
+                                   float *out_scale, int32_t *m_indices, int32_t *output_index,
+                                   int32_t *status, epd_stream_t stream) {
+    using namespace epd;
+    const int T = num_tokens, k = num_topk, H = hidden;
+    if (T < 0 || k < 0 || H <= 0) return EPD_ERR_INVALID_ARG;
+    if (capacity_rows < (int64_t)T * k) return EPD_ERR_INVALID_ARG;
+    int64_t row_bytes;
+    int scale_cols;
+    if (dtype == EPD_BF16) {
+        if (H % 8 != 0 || x_scale != nullptr || out_scale != nullptr) return EPD_ERR_INVALID_ARG;
+        row_bytes = 2 * (int64_t)H;
+        scale_cols = 0;
+    } else if (dtype == EPD_FP8_E4M3) {
+        if (H % 128 != 0) return EPD_ERR_INVALID_ARG;
+        if (((int64_t)T * k > 0 && x_scale == nullptr) || (capacity_rows > 0 && out_scale == nullptr))
+            return EPD_ERR_INVALID_ARG;
+        if (!aligned4(x_scale) || !aligned4(out_scale)) return EPD_ERR_INVALID_ARG;
+        row_bytes = H;
+        scale_cols = H / 128;
+    } else {
+        return EPD_ERR_INVALID_ARG;
+    }
+    PermuteArgs a;
+    const epd_status_t st = permute_common(a, x, row_bytes, topk_idx, T, k, num_experts,
+                                           expert_start_loc, workspace, capacity_rows, out,
+                                           m_indices, output_index, status);
+    if (st != EPD_OK) return st;
+    a.x_scale = reinterpret_cast<const uint32_t *>(x_scale);
+    a.scale_cols = scale_cols;
+    a.scale_col_major = 0;
+    a.scale_ld = 0;
+    a.out_scale = reinterpret_cast<uint32_t *>(out_scale);
+    a.e_begin = 0;
+    a.e_end = num_experts;
+    return permute_launch(a, T, k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" epd_status_t ep_permute_ex(const void *x, int64_t row_bytes, const void *x_scale,
+                                      const int64_t *topk_idx, int num_tokens, int num_topk,
+                                      int num_experts, const int32_t *expert_start_loc,
+                                      const void *workspace, int64_t capacity_rows,
+                                      const epd_permute_view_t *view, void *out, void *out_scale,
+                                      int32_t *m_indices, int32_t *output_index, int32_t *status,
+                                      epd_stream_t stream) {
+    using namespace epd;
+    if (view == nullptr) return EPD_ERR_INVALID_ARG;
+    const epd_permute_view_t v = *view;
+    if (v.expert_begin < 0 || v.expert_end > num_experts || v.expert_begin >= v.expert_end)
+        return EPD_ERR_INVALID_ARG;
+    if (v.scale_cols < 0 || (v.scale_col_major != 0 && v.scale_col_major != 1))
+        return EPD_ERR_INVALID_ARG;
+    if (v.scale_cols > 0) {
+        if ((num_tokens > 0 && num_topk > 0 && x_scale == nullptr) ||
+            (capacity_rows > 0 && out_scale == nullptr) || !aligned4(x_scale) || !aligned4(out_scale))
+            return EPD_ERR_INVALID_ARG;
+        if (v.scale_col_major && v.scale_ld < capacity_rows) return EPD_ERR_INVALID_ARG;
+    }
+    PermuteArgs a;
+    const epd_status_t st = permute_common(a, x, row_bytes, topk_idx, num_tokens, num_topk,
+                                           num_experts, expert_start_loc, workspace,
+                                           capacity_rows, out, m_indices, output_index, status);
+    if (st != EPD_OK) return st;
+    a.x_scale = static_cast<const uint32_t *>(x_scale);
+    a.scale_cols = v.scale_cols;
+    a.scale_col_major = v.scale_col_major;
+    a.scale_ld = v.scale_ld;
+    a.out_scale = static_cast<uint32_t *>(out_scale);
+    a.e_begin = v.expert_begin;
+    a.e_end = v.expert_end;
+    return permute_launch(a, num_tokens, num_topk, reinterpret_cast<cudaStream_t>(stream));
 }
