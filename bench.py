@@ -79,16 +79,18 @@ def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
 
 
 # ----------------------------------------------------------------------------- bytes of the path
-def algorithmic_bytes(case, P: int, M: int) -> dict:
+def algorithmic_bytes(case, P: int, M: int, T_rows=None) -> dict:
     """Minimum HBM bytes of each step: every row read once and written once per
-    pick, plus the index, weight and count traffic."""
+    pick, plus the index, weight and count traffic. T_rows: tokens whose row is
+    read by the permute (all of them unless a view leaves some without a pick)."""
     T, H, k, E, R = case.T, case.H, case.k, case.E, case.R
     fp8 = case.dtype == "fp8"
     b = 1 if fp8 else 2
-    sc = (H // 128) * 4 if fp8 else 0
+    sc = case.x_scale.shape[1] * 4 if case.x_scale is not None else 0
+    Tr = T if T_rows is None else T_rows
     layout = T * k * 8 + T * R + 3 * E * 4
     scan = 2 * E * 4 + 4
-    permute = T * H * b + T * sc + P * H * b + P * sc + T * k * 8 + T * k * 4 + M * 4
+    permute = Tr * H * b + Tr * sc + P * H * b + P * sc + T * k * 8 + T * k * 4 + M * 4
     unpermute = P * H * 2 + T * H * 2 + T * k * 4 + T * k * 4
     return dict(ep_dispatch_layout=layout, ep_scan_offsets=scan, ep_permute=permute,
                 ep_unpermute=unpermute)
@@ -258,7 +260,7 @@ def run_epd(args, rank, world, local):
     init_dist(world, "nccl")
     epd.load_library()
     name = args.workload
-    case = workloads.make_case(name, T=args.tokens)
+    case = workloads.make_case(name, T=args.tokens, scales=args.scales)
     T, H, k, E, R, N = case.T, case.H, case.k, case.E, case.R, case.N
     A = max(1, int(args.align))
     M = case.capacity if A == 1 else epd.aligned_capacity(T, k, E, A)
@@ -282,7 +284,16 @@ def run_epd(args, rank, world, local):
     start = torch.empty(E, dtype=torch.int32, device=dev)
     total = torch.empty(1, dtype=torch.int32, device=dev)
     out = torch.empty(M, H, dtype=x.dtype, device=dev)
-    out_scale = None if xs is None else torch.empty(M, H // 128, dtype=torch.float32, device=dev)
+    col = args.scale_layout == "col"
+    use_ex = col or args.scales != "f32" or args.view_rank is not None
+    v_begin, v_end = 0, E
+    if args.view_rank is not None:
+        v_begin, v_end = args.view_rank * (E // R), (args.view_rank + 1) * (E // R)
+    if xs is None:
+        out_scale = None
+    else:
+        C = xs.shape[1]
+        out_scale = torch.empty((C, M) if col else (M, C), dtype=xs.dtype, device=dev)
     m_idx = torch.empty(M, dtype=torch.int32, device=dev)
     out_idx = torch.empty(T, k, dtype=torch.int32, device=dev)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
@@ -298,9 +309,14 @@ def run_epd(args, rank, world, local):
                                          total_rows=total, stream=stream)) if A == 1 else
             (lambda: epd.ep_scan_offsets_aligned(per_e, A, status, expert_start_loc=start,
                                                  total_rows=total, stream=stream)),
-            lambda: epd.ep_permute(x, xs, topk, E, start, ws, status, capacity_rows=M, out=out,
-                                   out_scale=out_scale, m_indices=m_idx, output_index=out_idx,
-                                   stream=stream),
+            (lambda: epd.ep_permute(x, xs, topk, E, start, ws, status, capacity_rows=M, out=out,
+                                    out_scale=out_scale, m_indices=m_idx, output_index=out_idx,
+                                    stream=stream)) if not use_ex else
+            (lambda: epd.ep_permute_ex(x, xs, topk, E, start, ws, status, capacity_rows=M,
+                                       expert_begin=v_begin, expert_end=v_end,
+                                       scale_col_major=col, scale_ld=M if col else None,
+                                       out=out, out_scale=out_scale, m_indices=m_idx,
+                                       output_index=out_idx, stream=stream)),
             lambda: epd.ep_unpermute(out if eo is None else eo, out_idx, w, status, y=y,
                                      stream=stream),
         )
@@ -411,7 +427,8 @@ def run_epd(args, rank, world, local):
     achieved = bytes_k[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
     ms_per_step = ms / args.steps
     P = int((out_idx >= 0).sum().item())        # valid pairs (total is the padded row count)
-    bytes_k = algorithmic_bytes(case, P, M)
+    T_rows = int((out_idx >= 0).any(dim=1).sum().item())
+    bytes_k = algorithmic_bytes(case, P, M, T_rows)
     path_bytes = sum(bytes_k.values())
     path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
     kernels = {n: {"us": round(per_kernel_ms[n] * 1e3, 2), "bytes": bytes_k[n],
@@ -438,6 +455,9 @@ def run_epd(args, rank, world, local):
                    else "bf16",
                    "expert_out": "bf16 identity (permuted rows)" if eo is None else "bf16 seeded",
                    "capacity_rows": M, "valid_pairs": P, "expert_alignment": A,
+                   "scales": args.scales if case.dtype == "fp8" else None,
+                   "scale_layout": args.scale_layout if case.dtype == "fp8" else None,
+                   "experts_in_view": [v_begin, v_end],
                    "l2": f"no flush: {path_bytes / 1e6:.0f} MB moved per step > 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "hbm": {"path_gbs": round(path_gbs, 1), "path_bytes": path_bytes,
@@ -673,6 +693,12 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--align", type=int, default=1,
                     help="pad every expert's rows to a multiple of this (grouped-GEMM layout)")
+    ap.add_argument("--scales", choices=["f32", "ue8m0"], default="f32",
+                    help="fp8 scale words: fp32 per 128 columns, or UE8M0 exponents packed by 4")
+    ap.add_argument("--scale-layout", choices=["row", "col"], default="row",
+                    help="permuted scales row-major [M, C] or column-major [C, M]")
+    ap.add_argument("--view-rank", type=int, default=None,
+                    help="permute only this simulated rank's experts (local rows and ids)")
     ap.add_argument("--decode-pool", type=int, default=16,
                     help="distinct input sets cycled by the decode workload")
     args = ap.parse_args(argv)
