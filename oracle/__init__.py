@@ -76,6 +76,10 @@ def _load():
         lib.oracle_permute_ex.argtypes = [P, I64, P, I, I, I64, P, I, I, I, I, I, P, I64, P, P, P,
                                           P]
         lib.oracle_permute_ex.restype = I
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.oracle_permute_lowlatency.argtypes = [P, I, I, I, P, I, I, I, I64, P, P, P, P, P, P]
+        lib.oracle_permute_lowlatency.restype = I
         lib.oracle_unpermute.argtypes = [P, I64, P, P, I, I, I, P]
         lib.oracle_unpermute.restype = I
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
@@ -199,6 +203,39 @@ def permute_ex(x_rows, x_scale_words, topk_idx, num_experts: int, expert_start_l
                                    _ptr(m_indices), _ptr(output_index))
     _check(rc, "permute_ex")
     return dict(out=out, out_scale=out_scale, m_indices=m_indices, output_index=output_index)
+
+
+def e4m3_from_float(v: float) -> int:
+    return int(_load().oracle_e4m3_from_float(float(v)))
+
+
+def permute_lowlatency(x_bf16, topk_idx, num_experts: int, rows_per_expert: int,
+                       expert_begin: int = 0, expert_end=None):
+    """Fixed-rectangle layout with the fused cast. x_bf16: [T, H] uint16 (bf16 bits).
+    Returns dict(out_q [E_view, rows, H] uint8 (e4m3 bytes), out_scale [E_view, H/128,
+    rows] f32, recv_count [E_view] i32, output_index [T, k] i32, src_token
+    [E_view, rows] i32, overflow bool). Unwritten rows are zero (scales) / zero
+    bytes / -1 (src_token)."""
+    x = _c(x_bf16, np.uint16)
+    topk = _c(topk_idx, np.int64)
+    T, k = topk.shape
+    H = x.shape[1]
+    e_end = num_experts if expert_end is None else expert_end
+    EV = e_end - expert_begin
+    C = H // 128
+    out_q = np.zeros((EV, rows_per_expert, H), np.uint8)
+    out_scale = np.zeros((EV, C, rows_per_expert), np.float32)
+    recv = np.zeros(EV, np.int32)
+    oi = np.zeros((T, k), np.int32)
+    src = -np.ones((EV, rows_per_expert), np.int32)
+    ovf = ctypes.c_int(0)
+    rc = _load().oracle_permute_lowlatency(_ptr(x), T, k, H, _ptr(topk), num_experts,
+                                           int(expert_begin), int(e_end), int(rows_per_expert),
+                                           _ptr(out_q), _ptr(out_scale), _ptr(recv), _ptr(oi),
+                                           _ptr(src), ctypes.byref(ovf))
+    _check(rc, "permute_lowlatency")
+    return dict(out_q=out_q, out_scale=out_scale, recv_count=recv, output_index=oi,
+                src_token=src, overflow=bool(ovf.value))
 
 
 def unpermute(expert_out_bf16, output_index, topk_weights):

@@ -44,6 +44,8 @@ enum {
     ORC_ERR_CAPACITY = 6,
 };
 
+double oracle_double_from_bf16(uint16_t b);
+
 /* Simulated topology: [P2] "任务设定与数据流" places 2 experts on each of 8 GPUs
  * and the 8 GPUs on 2 nodes; contiguous blocks are the plain reading. */
 static int rank_of_expert(int64_t e, int E, int R) { return (int)(e / (E / R)); }
@@ -271,6 +273,100 @@ uint16_t oracle_bf16_from_double(double v) {
     uint32_t bits;
     memcpy(&bits, &f, sizeof bits);
     return (uint16_t)(sign | (uint16_t)((bits >> 16) & 0x7FFF));
+}
+
+/*
+ * float8 e4m3 (the "fn" variant: bias 7, 3 mantissa bits, largest finite 448,
+ * no infinities) from a float, round to nearest, ties to even, saturating to
+ * +-448; written from the format's definition (subnormal spacing 2^-9). NaN
+ * gives 0x7F.
+ */
+uint8_t oracle_e4m3_from_float(float v) {
+    if (isnan(v)) return (uint8_t)0x7F;
+    uint8_t sign = signbit(v) ? (uint8_t)0x80 : (uint8_t)0;
+    double a = fabs((double)v);
+    if (a == 0.0) return sign;
+    int ex;
+    (void)frexp(a, &ex);
+    int lead = ex - 1;
+    if (lead < -6) lead = -6;         /* below the normal range the spacing stays 2^-9 */
+    double spacing = ldexp(1.0, lead - 3);
+    double r = nearbyint(a / spacing) * spacing;
+    if (r > 448.0) r = 448.0;         /* saturate */
+    if (r == 0.0) return sign;
+    int rex;
+    (void)frexp(r, &rex);
+    int e = rex - 1;                  /* r in [2^e, 2^(e+1)) */
+    uint8_t bits;
+    if (e < -6) {                     /* subnormal: r = m * 2^-9, m in 1..7 */
+        bits = (uint8_t)(r / ldexp(1.0, -9));
+    } else {
+        int m = (int)((r / ldexp(1.0, e) - 1.0) * 8.0);
+        bits = (uint8_t)(((e + 7) << 3) | m);
+    }
+    return (uint8_t)(sign | bits);
+}
+
+/*
+ * Low-latency dispatch layout with the fused cast -- [P2] "3. 解决方案：固定矩形
+ * vs. 精确分配", strategy A (one fixed rectangle per expert, sized for the worst
+ * case, padded slots) and [P3] "low_latency模式" (low_latency_dispatch: bf16
+ * tokens cast to fp8 on the way, one fp32 scale per 128 columns with the last
+ * two dimensions column-major, recv_count per expert, per-row source info; no
+ * count exchange first). Experts [e_begin, e_end) each own rows_per_expert rows:
+ * the r-th pick of expert e in token-major order goes to row
+ * (e - e_begin) * rows_per_expert + r. A pick that finds its rectangle full is
+ * dropped (output_index -1) and *overflow is set.
+ *   cast, per token t and 128-column block c:
+ *     amax = max |x[t, 128c .. 128c+127]|,  scale = amax / 448 (fp32), 1 if amax = 0,
+ *     q[h] = e4m3(x[t, h] / scale) with the division in fp32;
+ *   out_q [E_view, rows_per_expert, H] e4m3 bytes; out_scale [E_view, H/128,
+ *   rows_per_expert] (column-major per expert); recv_count [E_view] = rows used;
+ *   src_token [E_view, rows_per_expert] = the token of each used row.
+ * Rows beyond recv_count are not written.
+ */
+int oracle_permute_lowlatency(const uint16_t *x, int T, int k, int H, const int64_t *topk_idx,
+                              int E, int e_begin, int e_end, int64_t rows_per_expert,
+                              uint8_t *out_q, float *out_scale, int32_t *recv_count,
+                              int32_t *output_index, int32_t *src_token, int *overflow) {
+    if (T < 0 || k < 0 || H <= 0 || H % 128 != 0 || E < 1 || rows_per_expert < 0)
+        return ORC_ERR_INVALID_ARG;
+    if (e_begin < 0 || e_end > E || e_begin >= e_end) return ORC_ERR_INVALID_ARG;
+    const int C = H / 128;
+    const int EV = e_end - e_begin;
+    *overflow = 0;
+    for (int e = 0; e < EV; ++e) recv_count[e] = 0;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t e = topk_idx[(int64_t)t * k + j];
+            if (e < -1 || e >= E) return ORC_ERR_INVALID_EXPERT;
+            output_index[(int64_t)t * k + j] = -1;
+            if (e < e_begin || e >= e_end) continue;
+            int64_t r = recv_count[e - e_begin];
+            if (r >= rows_per_expert) {
+                *overflow = 1;
+                continue;
+            }
+            recv_count[e - e_begin] += 1;
+            int64_t row = (e - e_begin) * rows_per_expert + r;
+            output_index[(int64_t)t * k + j] = (int32_t)row;
+            src_token[row] = t;
+            for (int c = 0; c < C; ++c) {
+                float amax = 0.0f;
+                for (int h = 128 * c; h < 128 * (c + 1); ++h) {
+                    float v = fabsf((float)oracle_double_from_bf16(x[(int64_t)t * H + h]));
+                    if (v > amax) amax = v;
+                }
+                float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+                out_scale[((e - e_begin) * (int64_t)C + c) * rows_per_expert + r] = scale;
+                for (int h = 128 * c; h < 128 * (c + 1); ++h) {
+                    float v = (float)oracle_double_from_bf16(x[(int64_t)t * H + h]);
+                    out_q[row * H + h] = oracle_e4m3_from_float(v / scale);
+                }
+            }
+        }
+    }
+    return ORC_OK;
 }
 
 double oracle_double_from_bf16(uint16_t b) {

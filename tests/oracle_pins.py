@@ -436,3 +436,94 @@ def check_views_tile_the_buffer(orc, topk, E, R, alignment=1):
         rows = v["output_index"][sel]
         assert np.array_equal(v["out"][rows], full["out"][rows + base])
     assert np.array_equal(oi_all, full["output_index"])
+
+
+# ----------------------------------------------------------------------------- low-latency layout
+def check_e4m3_rounding(orc, n=20000, seed=4):
+    """The oracle's e4m3 rounding against torch's float32 -> float8_e4m3fn conversion,
+    inside the finite range (torch does not saturate; the oracle clamps to 448)."""
+    rng = np.random.default_rng(seed)
+    v = np.concatenate([rng.uniform(-448, 448, n // 2),
+                        rng.standard_normal(n // 4) * 3,
+                        rng.uniform(-2 ** -6, 2 ** -6, n // 4)]).astype(np.float32)
+    # exact midpoints between neighbouring e4m3 values (ties) of every binade
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    mids = ((grid[:-1].astype(np.float64) + grid[1:]) / 2).astype(np.float32)
+    v = np.concatenate([v, mids, -mids, grid, -grid])
+    want = torch.from_numpy(v.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_from_float(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, want)
+    assert orc.e4m3_from_float(1e9) == 0x7E and orc.e4m3_from_float(-500.0) == 0xFE  # saturate
+
+
+def check_lowlatency_hand(orc):
+    """[P2] setting (E=16, top-2), rectangles of 2 rows: experts 3 and 7 each take two
+    picks, 0, 6 and 15 one; with 1 row per expert the second pick of 3 and of 7 is
+    dropped."""
+    topk = np.array([[3, 7], [3, -1], [0, 15], [7, 6]], np.int64)
+    x = np.zeros((4, 128), np.uint16)
+    r = orc.permute_lowlatency(x, topk, 16, 2)
+    assert r["output_index"].tolist() == [[6, 14], [7, -1], [0, 30], [15, 12]]
+    assert r["recv_count"].tolist() == [1, 0, 0, 2, 0, 0, 1, 2, 0, 0, 0, 0, 0, 0, 0, 1]
+    assert r["src_token"][3].tolist() == [0, 1] and r["src_token"][7].tolist() == [0, 3]
+    assert not r["overflow"]
+    r1 = orc.permute_lowlatency(x, topk, 16, 1)
+    assert r1["output_index"].tolist() == [[3, 7], [-1, -1], [0, 15], [-1, 6]]
+    assert r1["overflow"]
+    v = orc.permute_lowlatency(x, topk, 16, 2, expert_begin=6, expert_end=8)  # rank 3's view
+    assert v["output_index"].tolist() == [[-1, 2], [-1, -1], [-1, -1], [3, 0]]
+    assert v["recv_count"].tolist() == [1, 2]
+
+
+def check_lowlatency_cast_exact(orc):
+    """A block with amax 7 has scale 7/448 = 2^-6 exactly, so q = e4m3(64 x): values
+    whose 64x is an e4m3 value come back exactly; the amax maps to 448."""
+    vals = np.array([7.0, -7.0, 1.0, 0.5, -0.25, 3.5, 0.0, 2 ** -9], np.float32)
+    row = np.resize(vals, 256).astype(np.float32)
+    row[128:] = row[128:] * 0.5                         # second block: amax 3.5 -> 2^-7
+    xb = bf16_bits(torch.from_numpy(row).to(torch.bfloat16)).reshape(1, 256)
+    r = orc.permute_lowlatency(xb, np.array([[0]], np.int64), 1, 1)
+    assert r["out_scale"][0, :, 0].tolist() == [2.0 ** -6, 2.0 ** -7]
+    q = torch.from_numpy(r["out_q"][0, 0].copy()).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(q[:128], np.resize(vals * 64, 128).astype(np.float32).clip(-448, 448))
+    assert np.array_equal(q[128:], np.resize(vals * 64, 128).astype(np.float32).clip(-448, 448))
+    assert abs(q).max() == 448.0
+
+
+def check_lowlatency_against_exact_layout(orc, topk, E, rows, b=0, e_end=None, seed=0):
+    """Rectangle rows are the exact layout's rows shifted to fixed per-expert bases:
+    the r-th pick of expert e (token-major) sits at (e - b) * rows + r; the cast
+    dequantises to within e4m3's spacing."""
+    T, k = topk.shape
+    e_end = E if e_end is None else e_end
+    rng = np.random.default_rng(seed)
+    H = 256
+    xf = (rng.standard_normal((T, H)) * rng.uniform(0.01, 10, size=(T, 1))).astype(np.float32)
+    xb = bf16_bits(torch.from_numpy(xf).to(torch.bfloat16))
+    r = orc.permute_lowlatency(xb, topk, E, rows, b, e_end)
+    seen = Counter()
+    overflow = False
+    for t in range(T):
+        for j in range(k):
+            e = int(topk[t, j])
+            if not (b <= e < e_end):
+                assert r["output_index"][t, j] == -1
+                continue
+            rank = seen[e]
+            seen[e] += 1
+            if rank >= rows:
+                overflow = True
+                assert r["output_index"][t, j] == -1
+                continue
+            row = (e - b) * rows + rank
+            assert r["output_index"][t, j] == row
+            assert r["src_token"].reshape(-1)[row] == t
+            xs = (xb[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            q = torch.from_numpy(r["out_q"].reshape(-1, H)[row].copy()).view(
+                torch.float8_e4m3fn).double().numpy()
+            sc = r["out_scale"][e - b, :, rank].astype(np.float64)
+            deq = q * np.repeat(sc, 128)
+            tol = np.maximum(np.abs(xs) * 2.0 ** -4, np.repeat(sc, 128) * 2.0 ** -9) * 1.0001
+            assert np.all(np.abs(deq - xs) <= tol)
+    assert r["overflow"] == overflow
+    assert r["recv_count"].tolist() == [min(seen[e], rows) for e in range(b, e_end)]

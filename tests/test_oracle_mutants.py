@@ -11,7 +11,9 @@ import pytest
 import oracle as oracle_pkg
 from oracle_pins import (check_bf16_rounding, check_bruteforce, check_combine_all,
                          check_hand_example, check_hand_example_aligned,
-                         check_hand_example_rank3, check_invariants, check_view_against_reference)
+                         check_hand_example_rank3, check_invariants, check_view_against_reference,
+                         check_e4m3_rounding, check_lowlatency_hand, check_lowlatency_cast_exact,
+                         check_lowlatency_against_exact_layout)
 
 SRC = os.path.join(os.path.dirname(oracle_pkg.__file__), "epd_oracle.c")
 
@@ -38,6 +40,17 @@ MUTANTS = {
     "scale_col_major_swapped": ("if (scale_col_major) out_scale[(int64_t)c * scale_ld + s] = v;",
                                 "if (scale_col_major) out_scale[s * scale_ld + c] = v;"),
     "view_range_off_by_one": ("if (e < e_begin || e >= e_end) {", "if (e < e_begin || e > e_end) {"),
+    "e4m3_truncates": ("double r = nearbyint(a / spacing) * spacing;",
+                       "double r = floor(a / spacing) * spacing;"),
+    "e4m3_no_saturation": ("if (r > 448.0) r = 448.0;         /* saturate */", ""),
+    "cast_scale_not_divided": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                               "float scale = amax > 0.0f ? amax : 1.0f;"),
+    "cast_amax_signed": ("float v = fabsf((float)oracle_double_from_bf16(x[(int64_t)t * H + h]));",
+                         "float v = (float)oracle_double_from_bf16(x[(int64_t)t * H + h]);"),
+    "rectangle_overflow_kept": ("if (r >= rows_per_expert) {", "if (r > rows_per_expert) {"),
+    "rectangle_scale_row_major": (
+        "out_scale[((e - e_begin) * (int64_t)C + c) * rows_per_expert + r] = scale;",
+        "out_scale[((e - e_begin) * rows_per_expert + r) * (int64_t)C + c] = scale;"),
     "alignment_ignored": ("run += (c + alignment - 1) / alignment * alignment;", "run += c;"),
     "weight_wrong_index": ("acc += (double)topk_weights[(int64_t)t * k + j] *",
                            "acc += (double)topk_weights[(int64_t)t * k] *"),
@@ -83,6 +96,11 @@ def _run_pins(orc):
     check_hand_example_aligned(orc)
     check_bruteforce(orc, 2, 2, 4, 2, 1, limit=2000, alignment=4)
     check_hand_example_rank3(orc)
+    check_e4m3_rounding(orc, n=2000)
+    check_lowlatency_hand(orc)
+    check_lowlatency_cast_exact(orc)
+    t = np.array([[3, 7], [3, 1], [0, 15], [7, 6], [7, 3]], np.int64)
+    check_lowlatency_against_exact_layout(orc, t, 16, 2, 0, 16, seed=5)
     for flat in [(0, 3, 1, 2, -1, 3), (3, 3, 2, 1, 0, 0), (1, 2, 2, 3, 3, -1)]:
         t = np.array(flat, np.int64).reshape(3, 2)
         check_view_against_reference(orc, t, 4, 1, 4, 1, True)

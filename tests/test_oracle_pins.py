@@ -178,3 +178,29 @@ def test_views_on_workload_shapes():
     c = workloads.make_case("skew_bf16", T=300, experts="identity")
     for b, e in [(0, 8), (64, 72), (248, 256)]:
         check_view_against_reference(oracle, c.topk_idx.numpy(), c.E, b, e, 1, True)
+
+
+# ----------------------------------------------------------------------------- low-latency layout
+from oracle_pins import (check_e4m3_rounding, check_lowlatency_against_exact_layout,  # noqa: E402
+                         check_lowlatency_cast_exact, check_lowlatency_hand)
+
+
+def test_e4m3_rounding_matches_torch():
+    check_e4m3_rounding(oracle)
+
+
+def test_lowlatency_hand_example():
+    check_lowlatency_hand(oracle)
+
+
+def test_lowlatency_cast_exact_values():
+    check_lowlatency_cast_exact(oracle)
+
+
+@pytest.mark.parametrize("rows,b,e_end", [(64, 0, None), (3, 0, None), (40, 8, 16), (1, 4, 6)])
+def test_lowlatency_against_exact_layout(rows, b, e_end):
+    c = workloads.make_case("decode_fp8", seed=1001)
+    topk = c.topk_idx.numpy()
+    E = 32
+    topk = np.where(topk >= 0, topk % E, -1)
+    check_lowlatency_against_exact_layout(oracle, topk, E, rows, b, e_end, seed=rows)
