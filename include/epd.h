@@ -235,6 +235,38 @@ EPD_API epd_status_t ep_permute_ex(const void *x, int64_t row_bytes, const void 
                                    epd_stream_t stream);
 
 /*
+ * Low-latency dispatch layout with the fused cast. [P2] "3. 解决方案：固定矩形 vs.
+ * 精确分配" strategy A (a fixed rectangle of rows per expert, sized for the worst
+ * case, no count exchange first) and [P3] "low_latency模式" (low_latency_dispatch:
+ * bf16 tokens cast to fp8 e4m3 on the way, one fp32 scale per 128 columns with
+ * the last two dimensions column-major, recv_count, per-row source info).
+ * Experts [expert_begin, expert_end) each own rows_per_expert rows; the r-th pick
+ * of expert e in token-major order (the pair ranks ep_dispatch_layout left in
+ * `workspace`) goes to row (e - expert_begin) * rows_per_expert + r -- no
+ * ep_scan_offsets is needed. For every token with a pick in the view and every
+ * 128-column block c:
+ *   amax = max |x[t, 128c .. 128c+127]|, scale = amax / 448 (fp32; 1 if amax = 0),
+ *   q = e4m3(x / scale), fp32 division, round to nearest even, saturating at 448,
+ * written to every row the token goes to.
+ *   x_bf16:    [T, H] bfloat16, H % 128 == 0, 16-byte aligned;
+ *   out_q:     [E_view, rows_per_expert, H] e4m3 bytes, 8-byte aligned;
+ *   out_scale: [E_view, H/128, rows_per_expert] float32;
+ *   recv_count [E_view] int32: rows used per expert (at most rows_per_expert);
+ *   output_index [T, k] int32: row of each pair, -1 for no pick, other experts,
+ *     or a pick that found its rectangle full (EPD_ERR_CAPACITY in *status);
+ *   src_token [E_view, rows_per_expert] int32: token of each used row; may be NULL.
+ * Rows at and beyond recv_count are not written. ep_unpermute combines expert
+ * outputs laid out in the same rectangles.
+ */
+EPD_API epd_status_t ep_permute_lowlatency(const void *x_bf16, const int64_t *topk_idx,
+                                           int num_tokens, int num_topk, int hidden,
+                                           int num_experts, int expert_begin, int expert_end,
+                                           int64_t rows_per_expert, const void *workspace,
+                                           void *out_q, float *out_scale, int32_t *recv_count,
+                                           int32_t *output_index, int32_t *src_token,
+                                           int32_t *status, epd_stream_t stream);
+
+/*
  * Step 4 -- unpermute (combine). [P3] "Dispatch" (combine is the reverse of
  * dispatch; topk_weights are fp32 [T, k]):
  *   y[t, h] = bf16( sum over j with output_index[t, j] != -1, in j order, of

@@ -350,3 +350,84 @@ def test_permute_ex_whole_range_equals_permute():
     assert np.array_equal(mi.cpu().numpy(), ref["m_indices"])
     rows = ref["output_index"][ref["output_index"] >= 0]
     assert np.array_equal(row_bytes(out)[rows], ref["out"][rows])
+
+
+# ----------------------------------------------------------------------------- low-latency layout
+def _ll_compare(case, rows, b=0, e_end=None, expect_status=0):
+    import oracle
+    dev = torch.device("cuda")
+    E = case.E
+    e_end = E if e_end is None else e_end
+    topk = case.topk_idx.to(dev)
+    x = case.x.to(dev)
+    ws = epd.new_workspace(case.T, case.k, E, case.R, case.N, dev)
+    st = epd.new_status(dev)
+    epd.ep_dispatch_layout(topk, E, case.R, case.N, ws, st)
+    q, sc, rc, oi, src = epd.ep_permute_lowlatency(x, topk, E, rows, ws, st, expert_begin=b,
+                                                   expert_end=e_end)
+    torch.cuda.synchronize()
+    assert int(st.item()) == expect_status
+    want = oracle.permute_lowlatency(bits16(case.x), case.topk_idx.numpy(), E, rows, b, e_end)
+    assert want["overflow"] == (expect_status == epd.EPD_ERR_CAPACITY)
+    got_oi = oi.cpu().numpy()
+    assert np.array_equal(got_oi, want["output_index"])
+    rcount = rc.cpu().numpy()
+    assert np.array_equal(rcount, want["recv_count"])
+    qb = q.cpu().view(torch.uint8).numpy().reshape(-1, case.H)
+    used = got_oi[got_oi >= 0]
+    assert np.array_equal(qb[used], want["out_q"].reshape(-1, case.H)[used])
+    gs = sc.cpu().numpy()
+    for e in range(e_end - b):
+        n = rcount[e]
+        assert np.array_equal(gs[e, :, :n], want["out_scale"][e, :, :n])
+        assert np.array_equal(src.cpu().numpy()[e, :n], want["src_token"][e, :n])
+    return oi, want
+
+
+def _bf16_decode_case(T=128, seed=3000, **kw):
+    return workloads.make_random_case(T=T, H=kw.pop("H", 7168), k=8, E=256, R=32, N=4,
+                                      dtype="bf16", seed=seed, routing=kw.pop("routing", "uniform"),
+                                      experts="random", **kw)
+
+
+def test_lowlatency_decode_shape():
+    case = _bf16_decode_case()
+    _ll_compare(case, rows=128)
+
+
+def test_lowlatency_rank_view():
+    case = _bf16_decode_case(T=300, seed=3001)
+    _ll_compare(case, rows=300, b=64, e_end=72)
+
+
+def test_lowlatency_overflow_is_reported_and_dropped():
+    case = _bf16_decode_case(T=200, seed=3002)
+    _ll_compare(case, rows=3, expect_status=epd.EPD_ERR_CAPACITY)
+
+
+@pytest.mark.parametrize("T", [0, 1, 33])
+@pytest.mark.parametrize("H", [128, 384])
+def test_lowlatency_edges(T, H):
+    case = _bf16_decode_case(T=T, seed=3003 + T, H=H, routing="repeats", p_invalid=0.3)
+    _ll_compare(case, rows=max(T, 1))
+
+
+def test_lowlatency_prefill_size():
+    case = _bf16_decode_case(T=2048, seed=3004)
+    _ll_compare(case, rows=256)
+
+
+def test_combine_over_rectangles():
+    import oracle
+    case = _bf16_decode_case(T=128, seed=3005)
+    oi, want = _ll_compare(case, rows=128)
+    dev = torch.device("cuda")
+    eo = torch.randn(256 * 128, case.H, generator=torch.Generator().manual_seed(7)).to(
+        torch.bfloat16)
+    st = epd.new_status(dev)
+    y = epd.ep_unpermute(eo.to(dev), oi, case.topk_weights.to(dev), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.unpermute(bits16(eo), want["output_index"], case.topk_weights.numpy())
+    from epd_paths import combine_error
+    assert combine_error(bits16(y), ref) <= 1.0

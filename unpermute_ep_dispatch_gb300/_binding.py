@@ -54,6 +54,8 @@ SIGNATURES = {
     "ep_permute_ex": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _I64, ctypes.POINTER(PermuteView),
                            _P, _P, _P, _P, _P, _P]),
     "ep_unpermute": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "ep_permute_lowlatency": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P,
+                                   _P, _P]),
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "epd_test_layout_stalled_tile": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
                                           _U32, _P]),
@@ -335,6 +337,42 @@ def ep_permute_ex(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: to
                                       _stream(stream, dev))
     _check(rc, "ep_permute_ex")
     return out, out_scale, m_indices, output_index
+
+
+def ep_permute_lowlatency(x: torch.Tensor, topk_idx: torch.Tensor, num_experts: int,
+                          rows_per_expert: int, workspace: torch.Tensor, status: torch.Tensor,
+                          expert_begin: int = 0, expert_end: Optional[int] = None, out_q=None,
+                          out_scale=None, recv_count=None, output_index=None, src_token=None,
+                          with_src_token: bool = True, stream=None):
+    """Fixed-rectangle layout with the fused bf16 -> e4m3 cast (see epd.h).
+    x: [T, H] bfloat16. Returns (out_q [E_view, rows, H] float8_e4m3fn, out_scale
+    [E_view, H/128, rows] f32, recv_count [E_view] i32, output_index [T, k] i32,
+    src_token [E_view, rows] i32 or None)."""
+    _want(x, "x", torch.bfloat16)
+    dev = x.device
+    T, H = x.shape
+    _want(topk_idx, "topk_idx", torch.int64, device=dev)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, k] with the T of x")
+    k = topk_idx.shape[1]
+    E = int(num_experts)
+    e_end = E if expert_end is None else int(expert_end)
+    EV = e_end - int(expert_begin)
+    rows = int(rows_per_expert)
+    _want(workspace, "workspace", torch.uint8, device=dev)
+    _want(status, "status", torch.int32, (1,), dev)
+    out_q = _out(out_q, "out_q", torch.float8_e4m3fn, (EV, rows, H), dev)
+    out_scale = _out(out_scale, "out_scale", torch.float32, (EV, H // 128, rows), dev)
+    recv_count = _out(recv_count, "recv_count", torch.int32, (EV,), dev)
+    output_index = _out(output_index, "output_index", torch.int32, (T, k), dev)
+    if with_src_token:
+        src_token = _out(src_token, "src_token", torch.int32, (EV, rows), dev)
+    rc = load_library().ep_permute_lowlatency(
+        _ptr(x), _ptr(topk_idx), T, k, H, E, int(expert_begin), e_end, rows, _ptr(workspace),
+        _ptr(out_q), _ptr(out_scale), _ptr(recv_count), _ptr(output_index), _ptr(src_token),
+        _ptr(status), _stream(stream, dev))
+    _check(rc, "ep_permute_lowlatency")
+    return out_q, out_scale, recv_count, output_index, src_token
 
 
 def ep_unpermute(expert_out: torch.Tensor, output_index: torch.Tensor,

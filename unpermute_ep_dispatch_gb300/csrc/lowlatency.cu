@@ -1,0 +1,196 @@
+// lowlatency.cu -- the fixed-rectangle (low-latency) dispatch layout with the
+// fused bf16 -> fp8 cast.
+//
+// "高性能专家并行（EP）内核解剖学解读", section "3. 解决方案：固定矩形 vs. 精确分配",
+// strategy A: every expert owns a fixed rectangle of rows sized for the worst
+// case, so no count has to be exchanged before the rows move.
+// "[MoE] Deepseek的All-to-all通信: DeepEP代码解读", section "low_latency模式"
+// (low_latency_dispatch): bf16 tokens are cast to fp8 on the way, one fp32 scale
+// per 128 columns, the scales' last two dimensions column-major, recv_count per
+// expert and the source of every received row.
+//
+// The r-th pick of expert e (token-major order: the pair ranks left in the
+// workspace by ep_dispatch_layout) goes to row (e - e_begin) * rows + r; no
+// offset scan is needed. Work units are (token, two 128-column blocks); a
+// half-warp owns one block: 16-byte bf16 loads, the block's absolute maximum by
+// half-warp shuffles, scale = amax / 448 and q = e4m3(x / scale) with IEEE
+// divisions and the saturating round-to-nearest-even conversion, then 8-byte
+// stores of the quantised block to each row the token goes to.
+#include <cuda_fp8.h>
+
+#include "epd_common.cuh"
+
+namespace epd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct LLArgs {
+    const uint8_t *x;  // bf16 [T, H]
+    int T, k, H, E, e_begin, e_end;
+    int64_t rows;      // rows per expert rectangle
+    const int64_t *topk;
+    const int32_t *pair_rank;
+    const int32_t *counts;
+    const WsHeader *hdr;
+    uint8_t *out_q;      // e4m3 [E_view, rows, H]
+    float *out_scale;    // [E_view, H/128, rows]
+    int32_t *recv_count;
+    int32_t *output_index;
+    int32_t *src_token;  // [E_view, rows] or null
+    int32_t *status;
+};
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
+    __shared__ int s_row[kWarps][EPD_MAX_TOPK];
+    __shared__ int s_ok;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();  // pair ranks and counts come from the layout kernel
+    if (threadIdx.x == 0) {
+        s_ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
+        if (!s_ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    if (blockIdx.x == 0)
+        for (int e = threadIdx.x; e < a.e_end - a.e_begin; e += kThreads) {
+            const int64_t c = a.counts[a.e_begin + e];
+            a.recv_count[e] = (int32_t)(c < a.rows ? c : a.rows);
+        }
+
+    const int C = a.H >> 7;                // 128-column blocks per row
+    const int upt = (C + 1) >> 1;          // units (block pairs) per token
+    const int64_t units = (int64_t)a.T * upt;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t u_end = units * (gw + 1) / nw;
+    const int half = lane >> 4, hl = lane & 15;
+    int cur_t = -1;
+    bool any = false;
+    for (int64_t u = units * gw / nw; u < u_end; ++u) {
+        const int t = (int)(u / upt);
+        const int ch = (int)(u - (int64_t)t * upt);
+        if (t != cur_t) {
+            cur_t = t;
+            int has = 0;
+            __syncwarp();
+            for (int j = lane; j < a.k; j += 32) {
+                const int64_t idx = (int64_t)t * a.k + j;
+                const int64_t e = a.topk[idx];
+                int row = -1;
+                if (e >= a.e_begin && e < a.e_end) {
+                    const int64_t r = a.pair_rank[idx];
+                    if (r >= 0 && r < a.rows) {
+                        row = (int)((e - a.e_begin) * a.rows + r);
+                        if (ch == 0 && a.src_token) a.src_token[row] = t;
+                    } else if (ch == 0) {
+                        report(a.status, EPD_ERR_CAPACITY);  // the rectangle is full
+                    }
+                }
+                if (ch == 0) a.output_index[idx] = row;
+                s_row[warp][j] = row;
+                has |= (row >= 0);
+            }
+            any = __any_sync(0xffffffffu, has);
+            __syncwarp();
+        }
+        if (!any) continue;
+        const int c = 2 * ch + half;       // this half-warp's block
+        const bool active = c < C;
+        float v[8];
+        float amax = 0.0f;
+        if (active) {
+            const uint4 raw = ld_stream16(a.x + ((int64_t)t * a.H + 128 * c + 8 * hl) * 2);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(w[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (!active) continue;
+        const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        uint2 q;
+        q.x = e4m3x4(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale), __fdiv_rn(v[2], scale),
+                     __fdiv_rn(v[3], scale));
+        q.y = e4m3x4(__fdiv_rn(v[4], scale), __fdiv_rn(v[5], scale), __fdiv_rn(v[6], scale),
+                     __fdiv_rn(v[7], scale));
+        for (int j = 0; j < a.k; ++j) {
+            const int row = s_row[warp][j];
+            if (row < 0) continue;
+            *reinterpret_cast<uint2 *>(a.out_q + (int64_t)row * a.H + 128 * c + 8 * hl) = q;
+            if (hl == 0) {
+                const int64_t el = row / a.rows, r = row - el * a.rows;
+                a.out_scale[(el * C + c) * a.rows + r] = scale;
+            }
+        }
+    }
+    pdl_trigger();
+}
+
+}  // namespace
+}  // namespace epd
+
+extern "C" epd_status_t ep_permute_lowlatency(const void *x_bf16, const int64_t *topk_idx,
+                                              int num_tokens, int num_topk, int hidden,
+                                              int num_experts, int expert_begin, int expert_end,
+                                              int64_t rows_per_expert, const void *workspace,
+                                              void *out_q, float *out_scale, int32_t *recv_count,
+                                              int32_t *output_index, int32_t *src_token,
+                                              int32_t *status, epd_stream_t stream) {
+    using namespace epd;
+    const int T = num_tokens, k = num_topk, H = hidden, E = num_experts;
+    if (T < 0 || k < 0 || k > EPD_MAX_TOPK || E < 1 || E > EPD_MAX_EXPERTS) return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > INT32_MAX || H < 128 || H % 128 != 0) return EPD_ERR_INVALID_ARG;
+    if (expert_begin < 0 || expert_end > E || expert_begin >= expert_end) return EPD_ERR_INVALID_ARG;
+    const int64_t EV = expert_end - expert_begin;
+    if (rows_per_expert < 0 || EV * rows_per_expert > INT32_MAX) return EPD_ERR_INVALID_ARG;
+    if (!workspace || !recv_count || !status || !aligned16(workspace) || !aligned4(recv_count) ||
+        !aligned4(status))
+        return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > 0 && (!x_bf16 || !topk_idx || !output_index)) return EPD_ERR_INVALID_ARG;
+    if (EV * rows_per_expert > 0 && (!out_q || !out_scale)) return EPD_ERR_INVALID_ARG;
+    if ((x_bf16 && !aligned16(x_bf16)) || (topk_idx && !aligned8(topk_idx)) ||
+        (out_q && !aligned8(out_q)) || !aligned4(out_scale) || !aligned4(output_index) ||
+        !aligned4(src_token))
+        return EPD_ERR_INVALID_ARG;
+    const char *ws = static_cast<const char *>(workspace);
+    LLArgs a;
+    a.x = static_cast<const uint8_t *>(x_bf16);
+    a.T = T;
+    a.k = k;
+    a.H = H;
+    a.E = E;
+    a.e_begin = expert_begin;
+    a.e_end = expert_end;
+    a.rows = rows_per_expert;
+    a.topk = topk_idx;
+    a.pair_rank = reinterpret_cast<const int32_t *>(ws + ws_pair_rank_off());
+    a.counts = reinterpret_cast<const int32_t *>(ws + ws_counts_off(T, k));
+    a.hdr = reinterpret_cast<const WsHeader *>(ws);
+    a.out_q = static_cast<uint8_t *>(out_q);
+    a.out_scale = out_scale;
+    a.recv_count = recv_count;
+    a.output_index = output_index;
+    a.src_token = src_token;
+    a.status = status;
+    static int resident = 0;
+    if (resident == 0) resident = blocks_per_sm(lowlatency_kernel, kThreads, 0);
+    const int64_t units = (int64_t)T * ((H / 128 + 1) / 2);
+    const int64_t want = (units + kWarps - 1) / kWarps;
+    const int64_t full = (int64_t)sm_count() * resident;
+    const int grid = (int)(want < 1 ? 1 : (want < full ? want : full));
+    return launch_pdl(lowlatency_kernel, grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream),
+                      a);
+}
