@@ -501,10 +501,13 @@ def run_decode(args, rank, world, local):
     torch.cuda.set_device(dev)
     init_dist(world, "nccl")
     epd.load_library()
-    pool = [workloads.make_case("decode_fp8", seed=1000 + i) for i in range(args.decode_pool)]
+    ll = bool(args.lowlatency)
+    pool = [workloads.make_case("decode_fp8", seed=1000 + i, dtype="bf16" if ll else None)
+            for i in range(args.decode_pool)]
     c0 = pool[0]
     T, H, k, E, R, N = c0.T, c0.H, c0.k, c0.E, c0.R, c0.N
     M = T * k
+    rows = T  # low-latency rectangles: the worst case, every token on one expert
     stream = torch.cuda.Stream(dev)
     ws = epd.new_workspace(T, k, E, R, N, dev)
     status = epd.new_status(dev)
@@ -519,10 +522,34 @@ def run_decode(args, rank, world, local):
              m_idx=torch.empty(M, dtype=torch.int32, device=dev),
              out_idx=torch.empty(T, k, dtype=torch.int32, device=dev),
              y=torch.empty(T, H, dtype=torch.bfloat16, device=dev))
+    if ll:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(99)
+        o["q"] = torch.empty(E, rows, H, dtype=torch.float8_e4m3fn, device=dev)
+        o["qs"] = torch.empty(E, H // 128, rows, dtype=torch.float32, device=dev)
+        o["recv"] = torch.empty(E, dtype=torch.int32, device=dev)
+        o["src"] = torch.empty(E, rows, dtype=torch.int32, device=dev)
     inputs = [dict(topk=c.topk_idx.to(dev), w=c.topk_weights.to(dev), x=c.x.to(dev),
-                   xs=c.x_scale.to(dev), eo=c.expert_out.to(dev)) for c in pool]
+                   xs=None if c.x_scale is None else c.x_scale.to(dev),
+                   eo=(torch.randn(E * rows, H, generator=gen, device=dev).to(torch.bfloat16)
+                       if ll else c.expert_out.to(dev))) for c in pool]
+
+    def chain_ll(inp, ev=None):
+        epd.ep_dispatch_layout(inp["topk"], E, R, N, ws, status, tokens_per_expert=o["per_e"],
+                               tokens_per_rank=o["per_r"], tokens_per_rdma_rank=o["per_n"],
+                               is_token_in_rank=o["itr"], stream=stream)
+        epd.ep_permute_lowlatency(inp["x"], inp["topk"], E, rows, ws, status, out_q=o["q"],
+                                  out_scale=o["qs"], recv_count=o["recv"],
+                                  output_index=o["out_idx"], src_token=o["src"], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        epd.ep_unpermute(inp["eo"], o["out_idx"], inp["w"], status, y=o["y"], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
 
     def chain(inp, ev=None):
+        if ll:
+            return chain_ll(inp, ev)
         epd.ep_dispatch_layout(inp["topk"], E, R, N, ws, status, tokens_per_expert=o["per_e"],
                                tokens_per_rank=o["per_r"], tokens_per_rdma_rank=o["per_n"],
                                is_token_in_rank=o["itr"], stream=stream)
@@ -581,9 +608,14 @@ def run_decode(args, rank, world, local):
     lat = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
 
     # dominant kernel (largest bytes) timed with events on its stream, outside graphs
-    P = int(o["total"].item())
+    P = int((o["out_idx"] >= 0).sum().item())
     bytes_k = algorithmic_bytes(c0, P, M)
     names = ["ep_dispatch_layout", "ep_scan_offsets", "ep_permute", "ep_unpermute"]
+    if ll:  # no offset scan; the permute reads bf16 rows and writes e4m3 rows + scales
+        bytes_k.pop("ep_scan_offsets")
+        names.remove("ep_scan_offsets")
+        bytes_k["ep_permute"] = (T * H * 2 + P * H + P * (H // 128) * 4 + T * k * 16 + E * 4
+                                 + P * 4)
     dom = max(names, key=lambda n: bytes_k[n])
     evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(min(steps, 100))]
@@ -601,7 +633,11 @@ def run_decode(args, rank, world, local):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded routing, rows and expert outputs; no dataset)",
-        "config": {"workload": "decode_fp8", "tokens": T, "hidden": H, "top_k": k, "experts": E,
+        "config": {"workload": "decode_fp8" + ("_lowlatency" if ll else ""), "tokens": T,
+                   "hidden": H, "top_k": k, "experts": E,
+                   "path": ("layout -> fixed-rectangle permute with bf16->e4m3 cast -> combine"
+                            if ll else "layout -> offsets -> permute -> combine"),
+                   "rows_per_expert": rows if ll else None,
                    "simulated_ranks": R, "simulated_rdma_nodes": N,
                    "rows": "fp8_e4m3 + f32 scale per 128 columns", "expert_out": "bf16 seeded",
                    "input_sets": len(pool), "launch": "one CUDA graph per input set, replayed",
@@ -618,11 +654,11 @@ def run_decode(args, rank, world, local):
                      "frac": round(bytes_k[dom] / (dom_us * 1e-6) / 1e9 / peak, 4),
                      "traffic": None, "algorithmic_bytes": bytes_k[dom],
                      "note": "latency-bound at this size; timed outside the graphs"},
-        "gpu_launches": 4 * steps,
+        "gpu_launches": (3 if ll else 4) * steps,
         "clocks": clocks.summary(),
         "e2e": None,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not ll:
         v, reps, sec = time_oracle("decode_fp8", T, args.cpu_seconds, seed=1000)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                   "sample": f"decode_fp8 step of T={T}, {reps} reps in "
@@ -699,6 +735,8 @@ def main(argv=None):
                     help="permuted scales row-major [M, C] or column-major [C, M]")
     ap.add_argument("--view-rank", type=int, default=None,
                     help="permute only this simulated rank's experts (local rows and ids)")
+    ap.add_argument("--lowlatency", action="store_true",
+                    help="decode: fixed-rectangle layout with the fused bf16->fp8 cast")
     ap.add_argument("--decode-pool", type=int, default=16,
                     help="distinct input sets cycled by the decode workload")
     args = ap.parse_args(argv)

@@ -180,7 +180,8 @@ def make_rows(g, T, H, dtype, scales="f32"):
 
 
 def make_case(name: str = "tiny", seed: Optional[int] = None, T: Optional[int] = None,
-              experts: Optional[str] = None, scales: str = "f32") -> Case:
+              experts: Optional[str] = None, scales: str = "f32",
+              dtype: Optional[str] = None) -> Case:
     """Build one named workload (see CONFIGS). ``T`` overrides the token count
     (smaller instances of the same routing shape); ``experts`` overrides the
     expert-output mode ("identity" or "random")."""
@@ -191,6 +192,8 @@ def make_case(name: str = "tiny", seed: Optional[int] = None, T: Optional[int] =
         cfg["T"] = int(T)
     if experts is not None:
         cfg["experts"] = experts
+    if dtype is not None:
+        cfg["dtype"] = dtype
     return make_random_case(T=cfg["T"], H=cfg["H"], k=cfg["k"], E=cfg["E"], R=cfg["R"],
                             N=cfg["N"], dtype=cfg["dtype"], seed=seed,
                             routing=cfg["routing"], p_invalid=cfg.get("p_invalid", 0.0),
