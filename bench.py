@@ -300,20 +300,30 @@ def run_epd(args, rank, world, local):
     torch.cuda.synchronize(dev)
 
     io0 = dict(topk=topk, w=w, x=x, xs=xs, eo=eo, y=y)
+    fused = not args.separate_offsets  # steps 1 and 2 in one launch
 
     def step(ev=None, around=(0, 1, 2, 3), io=None):
         """One pass of the path; with `ev`, events bracket the kernels in `around`.
         `io` selects the input / output buffers (double-buffered end to end)."""
         io = io0 if io is None else io
         topk, w, x, xs, eo, y = io["topk"], io["w"], io["x"], io["xs"], io["eo"], io["y"]
+        if fused:
+            first = (lambda: epd.ep_dispatch_layout_offsets(
+                topk, E, R, N, ws, status, alignment=A, tokens_per_expert=per_e,
+                tokens_per_rank=per_r, tokens_per_rdma_rank=per_n, is_token_in_rank=itr,
+                expert_start_loc=start, total_rows=total, stream=stream), lambda: None)
+        else:
+            first = (
+                lambda: epd.ep_dispatch_layout(topk, E, R, N, ws, status, tokens_per_expert=per_e,
+                                               tokens_per_rank=per_r, tokens_per_rdma_rank=per_n,
+                                               is_token_in_rank=itr, stream=stream),
+                (lambda: epd.ep_scan_offsets(per_e, status, expert_start_loc=start,
+                                             total_rows=total, stream=stream)) if A == 1 else
+                (lambda: epd.ep_scan_offsets_aligned(per_e, A, status, expert_start_loc=start,
+                                                     total_rows=total, stream=stream)))
         calls = (
-            lambda: epd.ep_dispatch_layout(topk, E, R, N, ws, status, tokens_per_expert=per_e,
-                                           tokens_per_rank=per_r, tokens_per_rdma_rank=per_n,
-                                           is_token_in_rank=itr, stream=stream),
-            (lambda: epd.ep_scan_offsets(per_e, status, expert_start_loc=start,
-                                         total_rows=total, stream=stream)) if A == 1 else
-            (lambda: epd.ep_scan_offsets_aligned(per_e, A, status, expert_start_loc=start,
-                                                 total_rows=total, stream=stream)),
+            first[0],
+            first[1],
             (lambda: epd.ep_permute(x, xs, topk, E, start, ws, status, capacity_rows=M, out=out,
                                     out_scale=out_scale, m_indices=m_idx, output_index=out_idx,
                                     stream=stream)) if not use_ex else
@@ -454,15 +464,23 @@ def run_epd(args, rank, world, local):
                "note": "copies of step i+1 / read-back of step i overlap step i's kernels"}
         epd.check_status(status, "e2e steps")
 
+    if fused:  # one launch computes steps 1 and 2
+        per_kernel_ms["ep_dispatch_layout_offsets"] = per_kernel_ms.pop("ep_dispatch_layout")
+        per_kernel_ms.pop("ep_scan_offsets")
+        names = ["ep_dispatch_layout_offsets", "ep_permute", "ep_unpermute"]
     # ---- roofline of the dominant kernel and of the whole path
     peak, peak_src = load_peaks()
     dom_src = {"ep_unpermute": "unpermute.cu", "ep_permute": "permute.cu",
-               "ep_dispatch_layout": "layout.cu", "ep_scan_offsets": "scan.cu"}[dom]
+               "ep_dispatch_layout": "layout.cu", "ep_scan_offsets": "scan.cu",
+               "ep_dispatch_layout_offsets": "layout.cu"}[dom]
     achieved = bytes_k[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
     ms_per_step = ms / args.steps
     P = int((out_idx >= 0).sum().item())        # valid pairs (total is the padded row count)
     T_rows = int((out_idx >= 0).any(dim=1).sum().item())
     bytes_k = algorithmic_bytes(case, P, M, T_rows)
+    if fused:
+        bytes_k["ep_dispatch_layout_offsets"] = (bytes_k.pop("ep_dispatch_layout")
+                                                 + bytes_k.pop("ep_scan_offsets"))
     path_bytes = sum(bytes_k.values())
     path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
     kernels = {n: {"us": round(per_kernel_ms[n] * 1e3, 2), "bytes": bytes_k[n],
@@ -492,6 +510,8 @@ def run_epd(args, rank, world, local):
                    "scales": args.scales if case.dtype == "fp8" else None,
                    "scale_layout": args.scale_layout if case.dtype == "fp8" else None,
                    "experts_in_view": [v_begin, v_end],
+                   "launches": "layout+offsets fused, permute, combine" if fused else
+                               "layout, offsets, permute, combine",
                    "l2": f"no flush: {path_bytes / 1e6:.0f} MB moved per step > 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "hbm": {"path_gbs": round(path_gbs, 1), "path_bytes": path_bytes,
@@ -504,7 +524,7 @@ def run_epd(args, rank, world, local):
         "kernels_note": f"{dom} timed inside the timed region (events on every {DOM_EVERY}th "
                         f"step); the others from a separate "
                         f"{n_prof}-step pass with events around every kernel",
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (3 if fused else 4) * args.steps,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
@@ -584,11 +604,21 @@ def run_decode(args, rank, world, local):
     def chain(inp, ev=None):
         if ll:
             return chain_ll(inp, ev)
-        epd.ep_dispatch_layout(inp["topk"], E, R, N, ws, status, tokens_per_expert=o["per_e"],
-                               tokens_per_rank=o["per_r"], tokens_per_rdma_rank=o["per_n"],
-                               is_token_in_rank=o["itr"], stream=stream)
-        epd.ep_scan_offsets(o["per_e"], status, expert_start_loc=o["start"],
-                            total_rows=o["total"], stream=stream)
+        if args.separate_offsets:
+            epd.ep_dispatch_layout(inp["topk"], E, R, N, ws, status,
+                                   tokens_per_expert=o["per_e"], tokens_per_rank=o["per_r"],
+                                   tokens_per_rdma_rank=o["per_n"], is_token_in_rank=o["itr"],
+                                   stream=stream)
+            epd.ep_scan_offsets(o["per_e"], status, expert_start_loc=o["start"],
+                                total_rows=o["total"], stream=stream)
+        else:
+            epd.ep_dispatch_layout_offsets(inp["topk"], E, R, N, ws, status,
+                                           tokens_per_expert=o["per_e"],
+                                           tokens_per_rank=o["per_r"],
+                                           tokens_per_rdma_rank=o["per_n"],
+                                           is_token_in_rank=o["itr"],
+                                           expert_start_loc=o["start"], total_rows=o["total"],
+                                           stream=stream)
         epd.ep_permute(inp["x"], inp["xs"], inp["topk"], E, o["start"], ws, status,
                        capacity_rows=M, out=o["out"], out_scale=o["out_scale"],
                        m_indices=o["m_idx"], output_index=o["out_idx"], stream=stream)
@@ -688,7 +718,7 @@ def run_decode(args, rank, world, local):
                      "frac": round(bytes_k[dom] / (dom_us * 1e-6) / 1e9 / peak, 4),
                      "traffic": None, "algorithmic_bytes": bytes_k[dom],
                      "note": "latency-bound at this size; timed outside the graphs"},
-        "gpu_launches": (3 if ll else 4) * steps,
+        "gpu_launches": (3 if ll or not args.separate_offsets else 4) * steps,
         "clocks": clocks.summary(),
         "e2e": None,
     }
@@ -769,6 +799,8 @@ def main(argv=None):
                     help="permuted scales row-major [M, C] or column-major [C, M]")
     ap.add_argument("--view-rank", type=int, default=None,
                     help="permute only this simulated rank's experts (local rows and ids)")
+    ap.add_argument("--separate-offsets", action="store_true",
+                    help="run ep_dispatch_layout and ep_scan_offsets as two launches")
     ap.add_argument("--lowlatency", action="store_true",
                     help="decode: fixed-rectangle layout with the fused bf16->fp8 cast")
     ap.add_argument("--decode-pool", type=int, default=16,

@@ -134,6 +134,23 @@ EPD_API epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens,
                                 void *workspace, int32_t *status, epd_stream_t stream);
 
 /*
+ * Steps 1 and 2 in one launch: ep_dispatch_layout, and the block that finishes
+ * the look-back last also writes expert_start_loc and *total_rows exactly as
+ * ep_scan_offsets_aligned(tokens_per_expert, alignment) would (alignment 1 gives
+ * ep_scan_offsets). Saves one launch and one kernel per pass; same arguments and
+ * errors as ep_dispatch_layout otherwise.
+ */
+EPD_API epd_status_t ep_dispatch_layout_offsets(const int64_t *topk_idx, int num_tokens,
+                                                int num_topk, int num_experts, int num_ranks,
+                                                int num_rdma_ranks, int32_t *tokens_per_expert,
+                                                int32_t *tokens_per_rank,
+                                                int32_t *tokens_per_rdma_rank,
+                                                uint8_t *is_token_in_rank, int alignment,
+                                                int32_t *expert_start_loc, int32_t *total_rows,
+                                                void *workspace, int32_t *status,
+                                                epd_stream_t stream);
+
+/*
  * Step 2 -- expert offsets. [P2] "5. 缓冲区布局与发送" (the first source starts
  * at 0, each next one where the previous ended) and [P1] 2.2.4 (ep_scatter
  * scans, then scatters): expert_start_loc[e] = sum of tokens_per_expert[e'] for

@@ -431,3 +431,30 @@ def test_combine_over_rectangles():
     ref = oracle.unpermute(bits16(eo), want["output_index"], case.topk_weights.numpy())
     from epd_paths import combine_error
     assert combine_error(bits16(y), ref) <= 1.0
+
+
+# ----------------------------------------------------------------------------- fused layout + offsets
+@pytest.mark.parametrize("alignment", [1, 128])
+@pytest.mark.parametrize("name,T", [("dsv3_fp8", None), ("skew_bf16", 3000), ("tiny", None),
+                                    ("decode_fp8", None), ("prefill_bf16", 0)])
+def test_fused_layout_offsets_match_separate_steps(name, T, alignment):
+    case = workloads.make_case(name, T=T)
+    g = GpuPath(case, alignment=alignment)
+    g.layout()
+    g.scan()
+    torch.cuda.synchronize()
+    ws2 = epd.new_workspace(case.T, case.k, case.E, case.R, case.N)
+    st2 = epd.new_status()
+    per_r, per_n, per_e, itr, start, total = epd.ep_dispatch_layout_offsets(
+        g.topk, case.E, case.R, case.N, ws2, st2, alignment=alignment, with_rdma=True)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert torch.equal(per_e, g.per_e) and torch.equal(per_r, g.per_r)
+    assert torch.equal(per_n, g.per_n) and torch.equal(itr, g.itr)
+    assert torch.equal(start, g.start) and torch.equal(total, g.total)
+    # and the permute / combine on the fused layout's workspace match the oracle
+    g.ws = ws2
+    g.start.copy_(start)
+    g.permute()
+    g.unpermute()
+    compare(g.results(), oracle_path(case, alignment=alignment))

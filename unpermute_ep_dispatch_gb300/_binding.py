@@ -48,6 +48,8 @@ SIGNATURES = {
     "epd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "epd_workspace_init": (_I, [_P, _SZ, _P]),
     "ep_dispatch_layout": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "ep_dispatch_layout_offsets": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P,
+                                        _P, _P]),
     "ep_scan_offsets": (_I, [_P, _I, _P, _P, _P, _P]),
     "ep_scan_offsets_aligned": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "ep_permute": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
@@ -204,6 +206,43 @@ def ep_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
                                            _ptr(status), _stream(stream, dev))
     _check(rc, "ep_dispatch_layout")
     return per_r, per_n, per_e, itr
+
+
+def ep_dispatch_layout_offsets(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
+                               num_rdma_ranks: int, workspace: torch.Tensor, status: torch.Tensor,
+                               alignment: int = 1, tokens_per_expert=None, tokens_per_rank=None,
+                               tokens_per_rdma_rank=None, is_token_in_rank=None,
+                               expert_start_loc=None, total_rows=None,
+                               with_rdma: Optional[bool] = None,
+                               with_is_token_in_rank: bool = True, stream=None):
+    """Steps 1 and 2 in one launch. Returns (tokens_per_rank, tokens_per_rdma_rank or
+    None, tokens_per_expert, is_token_in_rank or None, expert_start_loc, total_rows)."""
+    _want(topk_idx, "topk_idx", torch.int64)
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [num_tokens, num_topk]")
+    dev = topk_idx.device
+    T, k = topk_idx.shape
+    E, R, N = int(num_experts), int(num_ranks), int(num_rdma_ranks)
+    _want(workspace, "workspace", torch.uint8, device=dev)
+    _want(status, "status", torch.int32, (1,), dev)
+    if workspace.numel() < epd_workspace_bytes(T, k, E, R, N):
+        raise ValueError("workspace too small for this layout")
+    if with_rdma is None:
+        with_rdma = N > 1 or tokens_per_rdma_rank is not None
+    per_e = _out(tokens_per_expert, "tokens_per_expert", torch.int32, (E,), dev)
+    per_r = _out(tokens_per_rank, "tokens_per_rank", torch.int32, (R,), dev)
+    per_n = _out(tokens_per_rdma_rank, "tokens_per_rdma_rank", torch.int32, (N,), dev) \
+        if with_rdma else None
+    itr = _out(is_token_in_rank, "is_token_in_rank", torch.bool, (T, R), dev) \
+        if with_is_token_in_rank else None
+    start = _out(expert_start_loc, "expert_start_loc", torch.int32, (E,), dev)
+    total = _out(total_rows, "total_rows", torch.int32, (1,), dev)
+    rc = load_library().ep_dispatch_layout_offsets(
+        _ptr(topk_idx), T, k, E, R, N, _ptr(per_e), _ptr(per_r), _ptr(per_n), _ptr(itr),
+        int(alignment), _ptr(start), _ptr(total), _ptr(workspace), _ptr(status),
+        _stream(stream, dev))
+    _check(rc, "ep_dispatch_layout_offsets")
+    return per_r, per_n, per_e, itr, start, total
 
 
 def ep_scan_offsets(tokens_per_expert: torch.Tensor, status: torch.Tensor,

@@ -48,6 +48,9 @@ struct LayoutArgs {
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
     int id_bits;  // bits needed for an expert id in [0, E)
+    int32_t *start_out;  // optional: expert offsets written by the last tile (fused step 2)
+    int32_t *total_out;
+    int alignment;
     int32_t *status;
     int stalled_tile;
     uint32_t spin_limit;
@@ -363,6 +366,42 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
             a.hdr->num_tokens = a.T;
             a.hdr->num_topk = a.k;
         }
+        if (a.start_out) {
+            // step 2 fused: exclusive prefix sum of the (padded) counts over the experts.
+            // Each thread owns a contiguous run of experts; warp-shuffle scan of the
+            // runs' sums, then of the warps' sums.
+            const int per = (a.E + kThreads - 1) / kThreads;
+            const int e0 = tid * per, e1 = min(a.E, e0 + per);
+            int run = 0;
+            for (int e = e0; e < e1; ++e)
+                run += (col_excl[e] + col_agg[e] + a.alignment - 1) / a.alignment * a.alignment;
+            int incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            __syncthreads();  // s_red is reused
+            if (lane == 31) s_red[warp] = incl;
+            __syncthreads();
+            if (warp == 0) {
+                const int v = lane < W ? s_red[lane] : 0;
+                int wincl = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, wincl, o);
+                    if (lane >= o) wincl += n;
+                }
+                if (lane < W) s_red[lane] = wincl - v;
+                if (lane == 31) *a.total_out = wincl;
+            }
+            __syncthreads();
+            int pos = s_red[warp] + incl - run;
+            for (int e = e0; e < e1; ++e) {
+                a.start_out[e] = pos;
+                pos += (col_excl[e] + col_agg[e] + a.alignment - 1) / a.alignment * a.alignment;
+            }
+        }
     }
 
     // (9) the last block to finish resets the call state for the next call
@@ -404,7 +443,8 @@ epd_status_t launch_layout(const LayoutArgs &a, size_t smem, cudaStream_t stream
     return launch_pdl(kernel, a.tiles, W * 32, smem, stream, a);
 }
 
-epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, int N,
+epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment,
+                           const int64_t *topk_idx, int T, int k, int E, int R, int N,
                            int32_t *per_expert, int32_t *per_rank, int32_t *per_node,
                            uint8_t *in_rank, void *workspace, int32_t *status, int stalled_tile,
                            uint32_t spin_limit, cudaStream_t stream) {
@@ -441,6 +481,9 @@ epd_status_t layout_launch(const int64_t *topk_idx, int T, int k, int E, int R, 
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
     a.tiles = w.tiles;
     a.tile_tokens = layout_tile_tokens(k);
+    a.start_out = start_out;
+    a.total_out = total_out;
+    a.alignment = alignment;
     a.id_bits = 0;
     while ((1 << a.id_bits) < E) ++a.id_bits;
     a.cols = w.cols;
@@ -522,10 +565,27 @@ epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens, int num
                                 int32_t *tokens_per_expert, int32_t *tokens_per_rank,
                                 int32_t *tokens_per_rdma_rank, uint8_t *is_token_in_rank,
                                 void *workspace, int32_t *status, epd_stream_t stream) {
-    return epd::layout_launch(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
+    return epd::layout_launch(nullptr, nullptr, 1, topk_idx, num_tokens, num_topk, num_experts, num_ranks,
                               num_rdma_ranks, tokens_per_expert, tokens_per_rank,
                               tokens_per_rdma_rank, is_token_in_rank, workspace, status, -1,
                               epd::kDefaultSpinLimit, reinterpret_cast<cudaStream_t>(stream));
+}
+
+epd_status_t ep_dispatch_layout_offsets(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                        int num_experts, int num_ranks, int num_rdma_ranks,
+                                        int32_t *tokens_per_expert, int32_t *tokens_per_rank,
+                                        int32_t *tokens_per_rdma_rank, uint8_t *is_token_in_rank,
+                                        int alignment, int32_t *expert_start_loc,
+                                        int32_t *total_rows, void *workspace, int32_t *status,
+                                        epd_stream_t stream) {
+    if (alignment < 1 || alignment > EPD_MAX_ALIGNMENT || !expert_start_loc || !total_rows ||
+        !epd::aligned4(expert_start_loc) || !epd::aligned4(total_rows))
+        return EPD_ERR_INVALID_ARG;
+    return epd::layout_launch(expert_start_loc, total_rows, alignment, topk_idx, num_tokens,
+                              num_topk, num_experts, num_ranks, num_rdma_ranks, tokens_per_expert,
+                              tokens_per_rank, tokens_per_rdma_rank, is_token_in_rank, workspace,
+                              status, -1, epd::kDefaultSpinLimit,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_tokens, int num_topk,
@@ -536,7 +596,7 @@ epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_token
                                           int32_t *status, int stalled_tile,
                                           uint32_t spin_limit, epd_stream_t stream) {
     if (stalled_tile < 0 || spin_limit > epd::kDefaultSpinLimit) return EPD_ERR_INVALID_ARG;
-    return epd::layout_launch(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
+    return epd::layout_launch(nullptr, nullptr, 1, topk_idx, num_tokens, num_topk, num_experts, num_ranks,
                               num_rdma_ranks, tokens_per_expert, tokens_per_rank,
                               tokens_per_rdma_rank, is_token_in_rank, workspace, status,
                               stalled_tile, spin_limit, reinterpret_cast<cudaStream_t>(stream));
@@ -599,7 +659,7 @@ extern "C" epd_status_t ep_dispatch_layout_noalloc(const int64_t *topk_idx, int 
     // counter that tags the look-back state carries over from the previous call.
     if (cudaMemsetAsync(scratch, 0, offsetof(WsHeader, epoch), s) != cudaSuccess)
         return record_cuda_error();
-    return layout_launch(topk_idx, T, k, num_experts, num_ranks, num_rdma_ranks,
+    return layout_launch(nullptr, nullptr, 1, topk_idx, T, k, num_experts, num_ranks, num_rdma_ranks,
                          tokens_per_expert, tokens_per_rank, tokens_per_rdma_rank,
                          is_token_in_rank, scratch, status, -1, kDefaultSpinLimit, s);
 }
