@@ -63,7 +63,7 @@ __device__ __forceinline__ int warp_sum(int v) {
 }
 
 template <int W>
-__global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
+__global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
     constexpr int kChunks = kLayoutTilePairs / kThreads;  // 32-pair chunks per warp
     extern __shared__ int4 smem_raw[];
@@ -90,12 +90,17 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
     }
     for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
     for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
-    pdl_wait();  // the workspace and topk_idx may come from the previous kernel
-    pdl_trigger();
+    // The ticket and the call counter are left by the previous call on this workspace,
+    // which has completed once the kernel before this one on the stream has started;
+    // topk_idx may come from that kernel, so it is read only after the wait. A call
+    // with one tile needs neither (no look-back, nothing to reset).
+    const bool multi = a.tiles > 1;
     if (tid == 0) {
-        s_tile = (int)atomicAdd(&a.hdr->ticket, 1u);
-        s_epoch = ld_relaxed_gpu(&a.hdr->epoch);
+        s_tile = multi ? (int)atomicAdd(&a.hdr->ticket, 1u) : 0;
+        s_epoch = multi ? ld_relaxed_gpu(&a.hdr->epoch) : 0u;
     }
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     const int tile = s_tile;
     const uint32_t epoch = s_epoch;
@@ -140,90 +145,106 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
         __syncwarp();
     }
 
-    // (3a) one thread per token: the ranks and nodes it reaches, as bit masks when
-    // R, N <= 64 (a token counts once per rank and once per node)
-    const bool small_r = a.R <= 64, small_n = a.N <= 64;
-    for (int tl = tid; tl < ntok; tl += kThreads) {
-        const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
-        unsigned long long rm = 0, nm = 0;
-        for (int j0 = 0; j0 < a.k; j0 += 8) {
-            int64_t vv[8];  // one batch of loads for up to 8 picks
-#pragma unroll
-            for (int q = 0; q < 8; ++q) vv[q] = (j0 + q < a.k) ? __ldg(row + j0 + q) : -1;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int j = j0 + q;
-                const int64_t v = vv[q];
-                if (v < 0 || v >= a.E) continue;
-                const int r = rank_of[v];
-                const int n = node_of[r];
-                if (small_r) {
-                    rm |= 1ull << r;
-                } else {
-                    bool new_r = true;
-                    for (int j2 = 0; j2 < j && new_r; ++j2) {
-                        const int64_t v2 = __ldg(row + j2);
-                        new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
-                    }
-                    if (new_r) atomicAdd(&col_agg[a.E + r], 1);
-                }
-                if (small_n) {
-                    nm |= 1ull << n;
-                } else {
-                    bool new_n = true;
-                    for (int j2 = 0; j2 < j && new_n; ++j2) {
-                        const int64_t v2 = __ldg(row + j2);
-                        new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
-                    }
-                    if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
-                }
-            }
-        }
-        tok_rmask[tl] = rm;
-        tok_nmask[tl] = nm;
-    }
     __syncthreads();
 
-    // (2) exclusive scan of the warp histograms per expert (warp-shuffle scan over
-    // the W warps), and the tile's count per expert
-    for (int e = warp; e < a.E; e += W) {
-        const int v = lane < W ? hw[lane * hws + e] : 0;
-        int incl = v;
+    // (2) exclusive scan of the warp histograms per expert: one thread per expert
+    // walks the W rows (consecutive experts are consecutive words: no bank
+    // conflicts), and the tile's count per expert
+    for (int e = tid; e < a.E; e += kThreads) {
+        constexpr int G = W < 8 ? W : 8;  // rows loaded per batch
+        int run = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
+        for (int w0 = 0; w0 < W; w0 += G) {
+            int v[G];
+#pragma unroll
+            for (int q = 0; q < G; ++q) v[q] = hw[(w0 + q) * hws + e];
+#pragma unroll
+            for (int q = 0; q < G; ++q) {
+                hw[(w0 + q) * hws + e] = run;
+                run += v[q];
+            }
         }
-        if (lane < W) hw[lane * hws + e] = incl - v;
-        if (lane == 31) col_agg[e] = incl;
+        col_agg[e] = run;
     }
-    // (3b) tokens per rank and per node from the masks: one thread per
-    // (rank or node, 32-token chunk)
-    const int nch = (ntok + 31) >> 5;
-    const int nr = small_r ? a.R : 0, nn = small_n ? a.N : 0;
-    for (int i = tid; i < nch * (nr + nn); i += kThreads) {
-        const int ch = i / (nr + nn), c = i - ch * (nr + nn);
-        const bool is_rank = c < nr;
-        const unsigned long long *m = is_rank ? tok_rmask : tok_nmask;
-        const int bit = is_rank ? c : c - nr;
-        int cnt = 0;
-        const int t_end = min(ntok, (ch + 1) * 32);
-        for (int t = ch * 32; t < t_end; ++t) cnt += (int)((m[t] >> bit) & 1ull);
-        if (cnt) atomicAdd(&col_agg[a.E + (is_rank ? bit : a.R + bit)], cnt);
+
+    // (3) one lane per token, warps taken from the top so that they run beside the
+    // scan above: the ranks and nodes the token reaches, as bit masks when
+    // R, N <= 64 (a token counts once per rank and once per node), and the tile's
+    // tokens per rank and per node from one ballot per mask bit
+    const bool small_r = a.R <= 64, small_n = a.N <= 64;
+    for (int base = (W - 1 - warp) * 32; base < ntok; base += kThreads) {
+        const int tl = base + lane;
+        unsigned long long rm = 0, nm = 0;
+        if (tl < ntok) {
+            const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+            for (int j0 = 0; j0 < a.k; j0 += 8) {
+                int64_t vv[8];  // one batch of loads for up to 8 picks
+#pragma unroll
+                for (int q = 0; q < 8; ++q) vv[q] = (j0 + q < a.k) ? __ldg(row + j0 + q) : -1;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = j0 + q;
+                    const int64_t v = vv[q];
+                    if (v < 0 || v >= a.E) continue;
+                    const int r = rank_of[v];
+                    const int n = node_of[r];
+                    if (small_r) {
+                        rm |= 1ull << r;
+                    } else {
+                        bool new_r = true;
+                        for (int j2 = 0; j2 < j && new_r; ++j2) {
+                            const int64_t v2 = __ldg(row + j2);
+                            new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
+                        }
+                        if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+                    }
+                    if (small_n) {
+                        nm |= 1ull << n;
+                    } else {
+                        bool new_n = true;
+                        for (int j2 = 0; j2 < j && new_n; ++j2) {
+                            const int64_t v2 = __ldg(row + j2);
+                            new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
+                        }
+                        if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
+                    }
+                }
+            }
+            tok_rmask[tl] = rm;
+            tok_nmask[tl] = nm;
+        }
+        // lane b of group g ends up with the warp's count for bit 32 g + b
+        for (int g = 0; g < 2; ++g) {
+            const int nb_r = small_r ? min(32, a.R - 32 * g) : 0;
+            const int nb_n = small_n ? min(32, a.N - 32 * g) : 0;
+            int cr = 0, cn = 0;
+            for (int b = 0; b < nb_r; ++b) {
+                const uint32_t m = __ballot_sync(0xffffffffu, (rm >> (32 * g + b)) & 1ull);
+                if (lane == b) cr = __popc(m);
+            }
+            for (int b = 0; b < nb_n; ++b) {
+                const uint32_t m = __ballot_sync(0xffffffffu, (nm >> (32 * g + b)) & 1ull);
+                if (lane == b) cn = __popc(m);
+            }
+            if (cr) atomicAdd(&col_agg[a.E + 32 * g + lane], cr);
+            if (cn) atomicAdd(&col_agg[a.E + a.R + 32 * g + lane], cn);
+        }
     }
     __syncthreads();
 
     // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its
     // prefix). The block barrier orders every thread's stores before thread 0's
     // release store of the state word.
-    const bool publish = (tile != a.stalled_tile);
+    const bool publish = multi && tile != a.stalled_tile;
     int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
     int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
-    for (int c = tid; c < a.cols; c += kThreads) {
-        if (tile == 0) my_incl[c] = col_agg[c];
-        else my_agg[c] = col_agg[c];
+    if (multi) {
+        for (int c = tid; c < a.cols; c += kThreads) {
+            if (tile == 0) my_incl[c] = col_agg[c];
+            else my_agg[c] = col_agg[c];
+        }
+        __syncthreads();
     }
-    __syncthreads();
     if (tid == 0 && publish)
         st_release_gpu(&a.state[tile], tag | (tile == 0 ? kStateIncl : kStateAgg));
 
@@ -324,10 +345,14 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
             if (wdone) break;
             pos -= 32;
         }
-        // (6) publish the inclusive prefix (later tiles may be waiting on it)
-        for (int c = tid; c < a.cols; c += kThreads) my_incl[c] = col_excl[c] + col_agg[c];
-        __syncthreads();
-        if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | kStateIncl);
+        // (6) publish the inclusive prefix. Tiles 1..32 reach the empty prefix before
+        // tile 0 inside their first window, so only a call with more than 33 tiles
+        // has a later tile that can stop on it (none needs it: aggregates suffice).
+        if (a.tiles > 33 && tile < a.tiles - 1) {
+            for (int c = tid; c < a.cols; c += kThreads) my_incl[c] = col_excl[c] + col_agg[c];
+            __syncthreads();
+            if (tid == 0 && publish) st_release_gpu(&a.state[tile], tag | kStateIncl);
+        }
     }
 
     // (7) rank of every pair inside its expert over the whole batch
@@ -406,7 +431,7 @@ __global__ void __launch_bounds__(W * 32) layout_kernel(LayoutArgs a) {
 
     // (9) the last block to finish resets the call state for the next call
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0 && multi) {
         const unsigned prev = atomicAdd(&a.hdr->done, 1u);
         if (prev == (unsigned)a.tiles - 1) {
             a.hdr->done = 0;
