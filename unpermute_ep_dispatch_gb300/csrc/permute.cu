@@ -49,20 +49,27 @@ struct PermuteArgs {
 // last expert whose region starts at or before s (experts that share a start have
 // empty regions), and holds that expert when it is among the region's first
 // count rows, else -1 (alignment padding, or rows after the last region). Works
-// for plain and aligned offsets alike; coalesced, one binary search per row.
-__device__ __forceinline__ void fill_m_indices(const PermuteArgs &a, int64_t base, int64_t first,
-                                               int64_t stride) {
-    for (int64_t s = first; s < a.capacity; s += stride) {
-        const int64_t g = s + base;  // row in the offsets' coordinates
-        int lo = a.e_begin, hi = a.e_end - 1;
-        while (lo < hi) {  // last e of the view with start[e] <= g
-            const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)__ldg(a.start + mid) <= g) lo = mid;
-            else hi = mid - 1;
-        }
-        const int64_t st = __ldg(a.start + lo);
-        a.m_indices[s] = (g >= st && g < st + __ldg(a.counts + lo)) ? lo - a.e_begin : -1;
+// for plain and aligned offsets alike. `seg_start` / `seg_count` are the view's
+// nseg offsets and counts (shared or global memory); g is the row in the
+// offsets' coordinates. Returns the expert relative to the view, or -1.
+__device__ __forceinline__ int row_expert(const int32_t *seg_start, const int32_t *seg_count,
+                                          int nseg, int64_t g) {
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {  // last segment with start <= g
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)seg_start[mid] <= g) lo = mid;
+        else hi = mid - 1;
     }
+    const int64_t st = seg_start[lo];
+    return (g >= st && g < st + seg_count[lo]) ? lo : -1;
+}
+
+__device__ __forceinline__ void fill_m_indices(const PermuteArgs &a, const int32_t *seg_start,
+                                               const int32_t *seg_count, int64_t base,
+                                               int64_t first, int64_t stride) {
+    const int nseg = a.e_end - a.e_begin;
+    for (int64_t s = first; s < a.capacity; s += stride)
+        a.m_indices[s] = row_expert(seg_start, seg_count, nseg, s + base);
 }
 
 // Row of the scale word c of buffer row s.
@@ -143,8 +150,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    fill_m_indices(a, base, (int64_t)blockIdx.x * kThreads + threadIdx.x,
-                   (int64_t)gridDim.x * kThreads);
+    fill_m_indices(a, a.start + a.e_begin, a.counts + a.e_begin, base,
+                   (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
 }
 
 // ----------------------------------------------------------------------------- bulk-copy variant
@@ -158,6 +165,7 @@ constexpr int kTmaThreads = 256;
 constexpr size_t kTmaStageBudget = 64 * 1024;  // shared memory for row stages (a few blocks per SM)
 constexpr int kTmaMaxStages = 16;
 constexpr uint32_t kTmaWaitLimit = 1u << 24;    // mbarrier polls before a wait gives up
+constexpr int kTmaSegMax = 1024;  // views of at most this many experts keep their offsets in shared memory
 
 __host__ __device__ inline int tma_batch_tokens(int k) {
     const int b = k > 0 ? 4096 / k : 512;
@@ -166,10 +174,10 @@ __host__ __device__ inline int tma_batch_tokens(int k) {
 
 struct TmaSmem {
     int stages;
-    size_t row_stride, slots_off, list_off, bars_off, total;
+    size_t row_stride, slots_off, list_off, bars_off, seg_off, total;  // seg_off 0: not staged
 };
 
-__host__ __device__ inline TmaSmem tma_smem(int64_t row_bytes, int k) {
+__host__ __device__ inline TmaSmem tma_smem(int64_t row_bytes, int k, int nseg) {
     TmaSmem m;
     m.row_stride = align_up((size_t)row_bytes, 128);
     const size_t fit = kTmaStageBudget / m.row_stride;
@@ -178,49 +186,79 @@ __host__ __device__ inline TmaSmem tma_smem(int64_t row_bytes, int k) {
     m.slots_off = (size_t)m.stages * m.row_stride;
     m.list_off = align_up(m.slots_off + (size_t)B * (k > 0 ? k : 1) * 4, 16);
     m.bars_off = align_up(m.list_off + (size_t)B * 4, 16);
-    m.total = m.bars_off + (size_t)m.stages * 8;
+    const size_t bars_end = m.bars_off + (size_t)m.stages * 8;
+    m.seg_off = nseg <= kTmaSegMax ? align_up(bars_end, 16) : 0;
+    m.total = m.seg_off ? m.seg_off + 2 * (size_t)nseg * 4 : bars_end;
     return m;
 }
 
 __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a) {
     extern __shared__ __align__(128) uint8_t tsm[];
     __shared__ int s_ok, s_n, s_failed;
-    const TmaSmem L = tma_smem(a.row_bytes, a.k);
+    const int nseg = a.e_end - a.e_begin;
+    const TmaSmem L = tma_smem(a.row_bytes, a.k, nseg);
     uint8_t *stage = tsm;
     int *s_slot = reinterpret_cast<int *>(tsm + L.slots_off);  // [batch tokens][k]
     int *s_list = reinterpret_cast<int *>(tsm + L.list_off);   // tokens of the batch with a slot
     uint64_t *bars = reinterpret_cast<uint64_t *>(tsm + L.bars_off);
+    int32_t *s_seg = reinterpret_cast<int32_t *>(tsm + L.seg_off);  // [nseg] offsets, [nseg] counts
     const int tid = threadIdx.x;
-    pdl_wait();  // offsets and pair ranks come from the previous kernels
-    if (tid == 0) {
-        const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
-        s_ok = ok;
-        s_failed = 0;
-        if (!ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
-        for (int i = 0; i < L.stages; ++i) mbar_init(&bars[i], 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-    if (!s_ok) return;
-    const int64_t base = a.start[a.e_begin];  // first row of the view in offset coordinates
-
     const int B = tma_batch_tokens(a.k);
     const int S = L.stages;
     const uint32_t bytes = (uint32_t)a.row_bytes;
     const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
     const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    // Over the whole expert range nearly every token is copied, so the block's first
+    // rows are loaded before their slots are known (a token without a valid pick is
+    // loaded and not stored); a view copies few of the tokens and loads after.
+    const bool whole = a.e_begin == 0 && a.e_end == a.E && a.k > 0;
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        mbar_init_fence();
+    }
+    pdl_wait();  // offsets and pair ranks come from the previous kernels
+    int pre = 0;  // rows of the first batch loaded ahead (thread 0)
+    if (tid == 0) {
+        if (whole) {
+            pre = min(S - 1, min(B, t_end - t_begin));
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(&bars[i], bytes);
+                bulk_load(stage + i * L.row_stride, a.x + (int64_t)(t_begin + i) * a.row_bytes,
+                          bytes, &bars[i]);
+            }
+        }
+        const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
+        s_ok = ok;
+        s_failed = 0;
+        if (!ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
+    }
+    // the view's offsets and counts, read once per block (slots and m_indices use them)
+    if (L.seg_off)
+        for (int i = tid; i < nseg; i += kTmaThreads) {
+            s_seg[i] = a.start[a.e_begin + i];
+            s_seg[nseg + i] = a.counts[a.e_begin + i];
+        }
+    __syncthreads();
+    if (!s_ok) {
+        if (tid == 0)  // loads issued ahead land before the block's shared memory is released
+            for (int i = 0; i < pre; ++i) mbar_wait_bounded(&bars[i], 0u, kTmaWaitLimit);
+        return;
+    }
+    const int32_t *seg_start = L.seg_off ? s_seg : a.start + a.e_begin;
+    const int32_t *seg_count = L.seg_off ? s_seg + nseg : a.counts + a.e_begin;
+    const int64_t base = seg_start[0];  // first row of the view in offset coordinates
+
     uint32_t seq = 0;  // rows this block has loaded so far: row r uses stage r % S, phase r / S
     for (int b0 = t_begin; b0 < t_end; b0 += B) {
         const int nb = min(B, t_end - b0);
-        if (tid == 0) s_n = 0;
-        __syncthreads();
+        if (tid == 0) s_n = 0;  // counted into after the next barrier
         for (int i = tid; i < nb * a.k; i += kTmaThreads) {
             const int tl = i / a.k;
             const int64_t idx = (int64_t)(b0 + tl) * a.k + (i - tl * a.k);
             const int64_t e = a.topk[idx];
             int s = -1;
             if (e >= a.e_begin && e < a.e_end) {
-                const int64_t sl = (int64_t)a.start[e] - base + a.pair_rank[idx];
+                const int64_t sl = (int64_t)seg_start[e - a.e_begin] - base + a.pair_rank[idx];
                 if (sl >= 0 && sl < a.capacity) {
                     s = (int)sl;
                 } else {
@@ -231,19 +269,22 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
             s_slot[i] = s;
         }
         __syncthreads();
-        for (int tl = tid; tl < nb; tl += kTmaThreads) {
-            bool any = false;
-            for (int j = 0; j < a.k; ++j) any |= s_slot[tl * a.k + j] >= 0;
-            if (any) s_list[atomicAdd(&s_n, 1)] = tl;  // copy order does not change the result
+        if (!whole) {
+            for (int tl = tid; tl < nb; tl += kTmaThreads) {
+                bool any = false;
+                for (int j = 0; j < a.k; ++j) any |= s_slot[tl * a.k + j] >= 0;
+                if (any) s_list[atomicAdd(&s_n, 1)] = tl;  // copy order does not change the result
+            }
+            __syncthreads();
         }
-        __syncthreads();
         if (tid == 0) {
-            const int n = s_n;
-            int issued = 0, landed = 0;
+            const int n = whole ? nb : s_n;
+            int issued = b0 == t_begin ? pre : 0, landed = 0;
+            auto token = [&](int i) { return whole ? i : s_list[i]; };
             auto load = [&](int i) {
                 const uint32_t r = seq + i, st = r % S;
                 mbar_expect_tx(&bars[st], bytes);
-                bulk_load(stage + st * L.row_stride, a.x + (int64_t)(b0 + s_list[i]) * a.row_bytes,
+                bulk_load(stage + st * L.row_stride, a.x + (int64_t)(b0 + token(i)) * a.row_bytes,
                           bytes, &bars[st]);
             };
             for (; issued < min(n, S - 1); ++issued) load(issued);
@@ -255,7 +296,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
                     break;
                 }
                 fence_proxy_async_smem();
-                const int *sl = s_slot + s_list[landed] * a.k;
+                const int *sl = s_slot + token(landed) * a.k;
                 for (int j = 0; j < a.k; ++j)
                     if (sl[j] >= 0)
                         bulk_store(a.out + (int64_t)sl[j] * a.row_bytes, stage + st * L.row_stride,
@@ -292,13 +333,13 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
         __syncthreads();
         if (s_failed) break;
     }
-    if (tid == 0) bulk_wait_all();
 
+    fill_m_indices(a, seg_start, seg_count, base, (int64_t)blockIdx.x * kTmaThreads + tid,
+                   (int64_t)gridDim.x * kTmaThreads);
+    if (tid == 0) bulk_wait_all();
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    fill_m_indices(a, base, (int64_t)blockIdx.x * kTmaThreads + tid,
-                   (int64_t)gridDim.x * kTmaThreads);
 }
 
 }  // namespace
@@ -309,7 +350,7 @@ namespace {
 
 epd_status_t permute_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs) {
     // bulk-copy kernel when at least two row stages fit in shared memory
-    const TmaSmem L = tma_smem(a.row_bytes, k);
+    const TmaSmem L = tma_smem(a.row_bytes, k, a.e_end - a.e_begin);
     if (L.stages >= 2) {
         static size_t opted = 0;
         if (L.total > opted) {
