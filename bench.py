@@ -285,6 +285,10 @@ def run_epd(args, rank, world, local):
     total = torch.empty(1, dtype=torch.int32, device=dev)
     out = torch.empty(M, H, dtype=x.dtype, device=dev)
     col = args.scale_layout == "col"
+    # ep_permute_ex adds its column-major scale pass for > 16 words per row over a
+    # view of at least a quarter of the experts
+    scale_pass = (col and xs is not None and xs.shape[1] > 16
+                  and (args.view_rank is None or 4 * (E // R) >= E))
     use_ex = col or args.scales != "f32" or args.view_rank is not None
     v_begin, v_end = 0, E
     if args.view_rank is not None:
@@ -524,7 +528,8 @@ def run_epd(args, rank, world, local):
         "kernels_note": f"{dom} timed inside the timed region (events on every {DOM_EVERY}th "
                         f"step); the others from a separate "
                         f"{n_prof}-step pass with events around every kernel",
-        "gpu_launches": (3 if fused else 4) * args.steps,
+        # column-major scales add the scale pass after the row copy (inside ep_permute_ex)
+        "gpu_launches": ((3 if fused else 4) + (1 if scale_pass else 0)) * args.steps,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }

@@ -241,7 +241,11 @@ typedef struct {
  * row_bytes (a multiple of 16) copied verbatim; `view` is a host pointer.
  * capacity_rows must hold the view's regions (a slot outside sets
  * EPD_ERR_CAPACITY). Otherwise as ep_permute, which is this call with the whole
- * expert range and row-major fp32 scales.
+ * expert range and row-major fp32 scales. With column-major scales of more than
+ * 16 words per row and a view of at least a quarter of the experts the call
+ * enqueues two kernels: the row copy, which parks each filled row's source token
+ * in m_indices, then a pass that writes the scales down their columns (coalesced)
+ * and the final m_indices; m_indices is only meaningful once both have run.
  */
 EPD_API epd_status_t ep_permute_ex(const void *x, int64_t row_bytes, const void *x_scale,
                                    const int64_t *topk_idx, int num_tokens, int num_topk,

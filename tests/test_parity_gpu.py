@@ -338,6 +338,61 @@ def test_permute_views_and_scale_layouts(scales, col_major, alignment):
             assert np.array_equal(gs[rows], want["out_scale"][rows])
 
 
+@pytest.mark.parametrize("shape", ["whole", "whole_aligned", "half_view", "wide_rows", "no_picks"])
+def test_permute_ex_column_major_scale_pass(shape):
+    """Column-major scales of more than 16 words per row over a view of at least a
+    quarter of the experts take the separate scale pass (the row copy parks each
+    filled row's source token in m_indices; the pass writes the scales down their
+    columns and the final m_indices). Rows, scales, m_indices and output_index equal
+    the oracle's, on the bulk-copy kernel and on the register kernel (rows wider
+    than two 32 KiB stages)."""
+    import oracle
+    alignment = 128 if shape == "whole_aligned" else 1
+    if shape == "wide_rows":
+        case = workloads.make_case("prefill_bf16", T=300)
+    else:
+        case = workloads.make_case("dsv3_fp8", T=2048)
+    if shape == "no_picks":
+        case = workloads.Case(**{**case.__dict__, "topk_idx": torch.full_like(case.topk_idx, -1)})
+    g = GpuPath(case, alignment=alignment)
+    g.layout()
+    g.scan()
+    torch.cuda.synchronize()
+    T, k, E = case.T, case.k, case.E
+    gen = torch.Generator().manual_seed(71)
+    if shape == "wide_rows":
+        x = torch.randint(0, 256, (T, 33024), generator=gen, dtype=torch.uint8)
+        words = torch.randint(-2**31, 2**31 - 1, (T, 40), generator=gen, dtype=torch.int32)
+    else:
+        x = case.x
+        words = case.x_scale.contiguous().view(torch.int32)
+    b, e = (0, E // 2) if shape == "half_view" else (0, E)
+    cap = oracle.aligned_capacity(T, k, E, alignment) if alignment > 1 else T * k
+    ld = cap + 12
+    lay = oracle.dispatch_layout(case.topk_idx.numpy(), E, case.R, case.N)
+    if alignment == 1:
+        ostart, _ = oracle.scan_offsets(lay["tokens_per_expert"])
+    else:
+        ostart, _ = oracle.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
+    assert np.array_equal(g.start.cpu().numpy(), ostart)
+    dx, dw = x.to(g.dev), words.to(g.dev)
+    out, osc, mi, oi = epd.ep_permute_ex(dx, dw, g.topk, E, g.start, g.ws, g.status,
+                                         capacity_rows=cap, expert_begin=b, expert_end=e,
+                                         scale_col_major=True, scale_ld=ld)
+    torch.cuda.synchronize()
+    assert int(g.status.item()) == 0
+    want = oracle.permute_ex(row_bytes(x), _words(words), case.topk_idx.numpy(), E, ostart, cap,
+                             expert_begin=b, expert_end=e, scale_col_major=True, scale_ld=ld)
+    got_oi = oi.cpu().numpy()
+    assert np.array_equal(got_oi, want["output_index"])
+    assert np.array_equal(mi.cpu().numpy(), want["m_indices"])
+    rows = got_oi[got_oi >= 0]
+    if shape == "no_picks":
+        assert rows.size == 0 and (mi.cpu().numpy() == -1).all()
+    assert np.array_equal(row_bytes(out)[rows], want["out"][rows])
+    assert np.array_equal(_words(osc)[:, rows], want["out_scale"][:, rows])
+
+
 def test_permute_ex_whole_range_equals_permute():
     case = workloads.make_case("prefill_bf16", T=1500)
     g = GpuPath(case)

@@ -43,6 +43,9 @@ struct PermuteArgs {
     int32_t *m_indices;
     int32_t *output_index;
     int32_t *status;
+    // column-major scales: the permute leaves each filled row's source token in
+    // m_indices and scale_gather_kernel writes the scales and the final m_indices
+    int defer_scales;
 };
 
 // m_indices over the whole buffer from the expert segments: row s belongs to the
@@ -116,7 +119,10 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
                     if (sl >= 0 && sl < a.capacity) s = (int)sl;
                     else if (ch == 0) report(a.status, EPD_ERR_CAPACITY);
                 }
-                if (ch == 0) a.output_index[idx] = s;
+                if (ch == 0) {
+                    a.output_index[idx] = s;
+                    if (s >= 0 && a.defer_scales) a.m_indices[s] = t;
+                }
                 s_slot[warp][j] = s;
                 has |= (s >= 0);
             }
@@ -136,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
             if (c0 < row_vecs) st16(dst + (c0 << 4), v0);
             if (c1 < row_vecs) st16(dst + (c1 << 4), v1);
         }
-        if (ch == 0) {  // fp8 scale row travels with chunk 0
+        if (ch == 0 && !a.defer_scales) {  // fp8 scale row travels with chunk 0
             for (int c = lane; c < a.scale_cols; c += 32) {
                 const uint32_t sv = a.x_scale[(int64_t)t * a.scale_cols + c];
                 for (int j = 0; j < a.k; ++j) {
@@ -150,8 +156,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
-    fill_m_indices(a, a.start + a.e_begin, a.counts + a.e_begin, base,
-                   (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    if (!a.defer_scales)
+        fill_m_indices(a, a.start + a.e_begin, a.counts + a.e_begin, base,
+                       (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
 }
 
 // ----------------------------------------------------------------------------- bulk-copy variant
@@ -266,6 +273,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
                 }
             }
             a.output_index[idx] = s;
+            if (s >= 0 && a.defer_scales) a.m_indices[s] = b0 + tl;
             s_slot[i] = s;
         }
         __syncthreads();
@@ -315,7 +323,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
             }
             seq += issued;
             bulk_wait_read<0>();  // stages are reused by the next batch
-        } else if (a.scale_cols > 0) {
+        } else if (a.scale_cols > 0 && !a.defer_scales) {
             // fp8 scale rows with plain loads and stores, while thread 0 streams rows
             const int nthreads = kTmaThreads - 32;
             const int t2 = tid - 32;
@@ -334,12 +342,64 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
         if (s_failed) break;
     }
 
-    fill_m_indices(a, seg_start, seg_count, base, (int64_t)blockIdx.x * kTmaThreads + tid,
-                   (int64_t)gridDim.x * kTmaThreads);
+    if (!a.defer_scales)
+        fill_m_indices(a, seg_start, seg_count, base, (int64_t)blockIdx.x * kTmaThreads + tid,
+                       (int64_t)gridDim.x * kTmaThreads);
     if (tid == 0) bulk_wait_all();
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
+}
+
+// ----------------------------------------------------------------------------- column-major scales
+// Scales whose buffer is column-major ([scale_cols][ld], the layout a TMA load of
+// one expert's scale tile wants) are written after the rows: scattered across
+// the permutation, every pick would store scale_cols words ld apart. Here one
+// thread owns one buffer row: it reads the row's source token (left in m_indices
+// by the permute), gathers that token's scale words (one cached row of x_scale)
+// and stores them down its column, so each warp-wide store covers 32 consecutive
+// rows of one column. It then writes the row's final m_indices.
+__global__ void __launch_bounds__(kThreads) scale_gather_kernel(PermuteArgs a) {
+    __shared__ int32_t s_seg[2 * kTmaSegMax];
+    __shared__ int s_ok;
+    const int tid = threadIdx.x;
+    const int nseg = a.e_end - a.e_begin;
+    const bool staged = nseg <= kTmaSegMax;
+    pdl_wait();  // source tokens come from the permute
+    if (tid == 0) s_ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
+    if (staged)
+        for (int i = tid; i < nseg; i += kThreads) {
+            s_seg[i] = a.start[a.e_begin + i];
+            s_seg[nseg + i] = a.counts[a.e_begin + i];
+        }
+    __syncthreads();
+    pdl_trigger();
+    if (!s_ok) return;  // the permute reported the workspace and wrote nothing
+    const int32_t *seg_start = staged ? s_seg : a.start + a.e_begin;
+    const int32_t *seg_count = staged ? s_seg + nseg : a.counts + a.e_begin;
+    const int64_t base = seg_start[0];
+    const int C = a.scale_cols;
+    for (int64_t s = (int64_t)blockIdx.x * kThreads + tid; s < a.capacity;
+         s += (int64_t)gridDim.x * kThreads) {
+        const int e = row_expert(seg_start, seg_count, nseg, s + base);
+        if (e >= 0) {
+            const int t = a.m_indices[s];
+            if (t >= 0 && t < a.T) {  // a permute that gave up early leaves rows unset
+                const uint32_t *src = a.x_scale + (int64_t)t * C;
+                uint32_t *dst = a.out_scale + s;
+                int c = 0;
+                for (; c + 8 <= C; c += 8) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = __ldg(src + c + q);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dst[(int64_t)(c + q) * a.scale_ld] = v[q];
+                }
+                for (; c < C; ++c) dst[(int64_t)c * a.scale_ld] = __ldg(src + c);
+            }
+        }
+        a.m_indices[s] = e;
+    }
 }
 
 }  // namespace
@@ -348,7 +408,24 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
 namespace epd {
 namespace {
 
+epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs);
+
 epd_status_t permute_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs) {
+    // The separate pass pays off when the scattered stores it replaces are many:
+    // more than 16 words per row (fp32 per-128 scales of a 4096-wide row and up;
+    // packed UE8M0 words of a 7168-wide row are 14) over a view holding at least a
+    // quarter of the experts (a narrow view fills few rows but the pass walks all).
+    a.defer_scales = a.scale_cols > 16 && a.scale_col_major && a.capacity > 0 &&
+                     4 * (int64_t)(a.e_end - a.e_begin) >= a.E;
+    const epd_status_t st = permute_rows_launch(a, T, k, cs);
+    if (st != EPD_OK || !a.defer_scales) return st;
+    const int64_t want = (a.capacity + kThreads - 1) / kThreads;
+    const int64_t full = 8 * (int64_t)sm_count();
+    const int grid = (int)(want < full ? want : full);
+    return launch_pdl(scale_gather_kernel, grid, kThreads, 0, cs, a);
+}
+
+epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs) {
     // bulk-copy kernel when at least two row stages fit in shared memory
     const TmaSmem L = tma_smem(a.row_bytes, k, a.e_end - a.e_begin);
     if (L.stages >= 2) {
