@@ -28,6 +28,15 @@
  *     caller's device word `status` with an atomic compare-and-swap from 0, so
  *     the first error sticks until the caller clears the word. Kernels never
  *     trap: the offending pair is skipped and the call completes.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the kernel before it on the stream drains, and waits
+ *     (griddepcontrol.wait) before it reads what that kernel may write; every
+ *     libepd kernel waits before it lets its own dependents start. The layout
+ *     calls take the workspace's tile ticket before that wait, so the kernel
+ *     launched immediately before them must not write the workspace, and a
+ *     workspace's previous call must be complete by the time the kernel before
+ *     the layout starts (always so when the kernels in between are libepd's or
+ *     were launched without programmatic serialization).
  *   - Sizes: T = num_tokens >= 0, k = num_topk in [0, EPD_MAX_TOPK],
  *     E = num_experts in [1, EPD_MAX_EXPERTS], R = num_ranks with E % R == 0,
  *     N = num_rdma_ranks with R % N == 0, T*k <= INT32_MAX.

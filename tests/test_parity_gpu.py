@@ -157,10 +157,12 @@ def test_deterministic_and_workspace_reuse():
 
 
 def test_workspace_shared_across_shapes():
-    """One workspace, sized for the largest shape, reused for smaller ones."""
+    """One workspace, sized for the largest shape, reused for smaller ones; one-tile
+    calls (which take no ticket and publish nothing) between many-tile calls leave the
+    ticket and call counter as the next many-tile call needs them."""
     big = workloads.make_case("dsv3_fp8", T=2048)
     ws = epd.new_workspace(2048, 8, 256, 32, 4)
-    for T in (2048, 17, 1500, 1):
+    for T in (2048, 17, 17, 1500, 1, 2048, 256):
         case = workloads.make_case("dsv3_fp8", T=T, seed=T)
         g = GpuPath(case)
         g.ws = ws[: epd.epd_workspace_bytes(T, 8, 256, 32, 4)]
