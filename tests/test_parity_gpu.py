@@ -88,6 +88,19 @@ def test_edge_fp8(T, k, E, R, N, H):
     compare(got, want)
 
 
+@pytest.mark.parametrize("T", [1, 300, 2100])
+@pytest.mark.parametrize("topo", [(16, 8, 2), (256, 32, 4)])
+def test_zero_topk(T, topo):
+    """k = 0: no pairs, zero counts and masks, an empty buffer and y = 0 (2100 tokens
+    are two layout tiles)."""
+    E, R, N = topo
+    case = workloads.make_random_case(T=T, H=136, k=0, E=E, R=R, N=N, dtype="bf16", seed=T,
+                                      routing="uniform", experts="random")
+    got, want, _ = run_both(case)
+    compare(got, want)
+    assert not got["y"].any()
+
+
 def test_large_topk_and_repeated_experts():
     """k = 64 (the limit) over 4 experts: long runs of the same expert in a row."""
     case = workloads.make_random_case(T=300, H=64, k=64, E=4, R=2, N=1, dtype="bf16", seed=4,

@@ -80,13 +80,17 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     __shared__ int s_tile;
     __shared__ uint32_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
-    __shared__ int s_red[W];
+    __shared__ int s_red[W], s_red2[W];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < W * hws; i += kThreads) hw[i] = 0;
     for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
+    }
+    for (int i = tid; i < a.tile_tokens; i += kThreads) {
+        tok_rmask[i] = 0;
+        tok_nmask[i] = 0;
     }
     for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
     for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
@@ -115,26 +119,80 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // is ranked: lanes holding the same expert find each other with one ballot per
     // bit of the expert id, and the lowest of them adds the group's size to the
     // warp's private histogram.
+    // A partial tile spreads its pairs over all warps: cpw chunks per warp, warp w
+    // owning pairs [32 cpw w, 32 cpw (w + 1)) (pairs stay in warp-major order, which
+    // the scan across warps relies on); chunks past the tile's last pair are skipped.
     int pe[kChunks], pr[kChunks];
-    const int p_base = warp * 32 * kChunks + lane;
+    const int cpw = max(1, min(kChunks, (npairs + kThreads - 1) / kThreads));
+    const int p_base = warp * 32 * cpw + lane;
+    const int live = min(cpw, max(0, (npairs - (p_base - lane) + 31) >> 5));
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int p = p_base + 32 * c;
         int64_t v = -1;
-        if (p < npairs) v = __ldg(a.topk + pair0 + p);
+        if (c < cpw && p < npairs) v = __ldg(a.topk + pair0 + p);
         pe[c] = (v >= 0 && v < a.E) ? (int)v : -1;
         if (v < -1 || v >= a.E) report(a.status, EPD_ERR_INVALID_EXPERT);
+    }
+    // the ranks and nodes each token reaches, as bit masks when R, N <= 64 (a token
+    // counts once per rank and once per node), from the picks already in registers:
+    // a token's picks sit in consecutive lanes, so a segmented OR scan over the
+    // chunk leaves its mask in the segment's last lane, which merges it into shared
+    // memory (a token cut by a chunk boundary has two such lanes)
+    const bool small_r = a.R <= 64, small_n = a.N <= 64;
+    if ((small_r || small_n) && a.k > 0) {
+        const bool packed = a.R <= 32 && a.N <= 32;  // rank bits low, node bits high
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+            if (c >= live) break;
+            const int p = p_base + 32 * c;
+            const int e = pe[c];
+            const int tl = p / a.k;
+            const int first = max(0, lane - (p - tl * a.k));  // lane of the segment's first pick
+            unsigned long long rm = 0, nm = 0;
+            if (e >= 0) {
+                const int r = rank_of[e];
+                if (packed) {
+                    rm = (1ull << r) | (1ull << (32 + node_of[r]));
+                } else {
+                    if (small_r) rm = 1ull << r;
+                    if (small_n) nm = 1ull << node_of[r];
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long ur = __shfl_up_sync(0xffffffffu, rm, o);
+                if (lane - o >= first) rm |= ur;
+                if (!packed) {
+                    const unsigned long long un = __shfl_up_sync(0xffffffffu, nm, o);
+                    if (lane - o >= first) nm |= un;
+                }
+            }
+            const bool last = lane == 31 || (p + 1) % a.k == 0;
+            if (last && tl < ntok) {
+                if (packed) {
+                    if (rm) {
+                        atomicOr(&tok_rmask[tl], rm & 0xffffffffull);
+                        atomicOr(&tok_nmask[tl], rm >> 32);
+                    }
+                } else {
+                    if (rm) atomicOr(&tok_rmask[tl], rm);
+                    if (nm) atomicOr(&tok_nmask[tl], nm);
+                }
+            }
+        }
     }
     int *my_hist = hw + warp * hws;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
+        pr[c] = 0;
+        if (c >= live) continue;
         const int e = pe[c];
         uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
         for (int b = 0; b < a.id_bits; ++b) {
             const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
             peers &= ((e >> b) & 1) ? set : ~set;
         }
-        pr[c] = 0;
         if (e >= 0) {
             const int before = __popc(peers & lanemask_lt());
             const int base = my_hist[e];
@@ -168,50 +226,34 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     }
 
     // (3) one lane per token, warps taken from the top so that they run beside the
-    // scan above: the ranks and nodes the token reaches, as bit masks when
-    // R, N <= 64 (a token counts once per rank and once per node), and the tile's
-    // tokens per rank and per node from one ballot per mask bit
-    const bool small_r = a.R <= 64, small_n = a.N <= 64;
+    // scan above: the tile's tokens per rank and per node from one ballot per mask
+    // bit; for R or N above 64 (no masks) each token counts its distinct ranks or
+    // nodes by comparing its picks
     for (int base = (W - 1 - warp) * 32; base < ntok; base += kThreads) {
         const int tl = base + lane;
         unsigned long long rm = 0, nm = 0;
         if (tl < ntok) {
-            const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
-            for (int j0 = 0; j0 < a.k; j0 += 8) {
-                int64_t vv[8];  // one batch of loads for up to 8 picks
-#pragma unroll
-                for (int q = 0; q < 8; ++q) vv[q] = (j0 + q < a.k) ? __ldg(row + j0 + q) : -1;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = j0 + q;
-                    const int64_t v = vv[q];
+            if (small_r) rm = tok_rmask[tl];
+            if (small_n) nm = tok_nmask[tl];
+            if (!small_r || !small_n) {
+                const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+                for (int j = 0; j < a.k; ++j) {
+                    const int64_t v = __ldg(row + j);
                     if (v < 0 || v >= a.E) continue;
                     const int r = rank_of[v];
                     const int n = node_of[r];
-                    if (small_r) {
-                        rm |= 1ull << r;
-                    } else {
-                        bool new_r = true;
-                        for (int j2 = 0; j2 < j && new_r; ++j2) {
-                            const int64_t v2 = __ldg(row + j2);
-                            new_r = !(v2 >= 0 && v2 < a.E && rank_of[v2] == r);
-                        }
-                        if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+                    bool new_r = !small_r, new_n = !small_n;
+                    for (int j2 = 0; j2 < j && (new_r || new_n); ++j2) {
+                        const int64_t v2 = __ldg(row + j2);
+                        if (v2 < 0 || v2 >= a.E) continue;
+                        const int r2 = rank_of[v2];
+                        if (r2 == r) new_r = false;
+                        if (node_of[r2] == n) new_n = false;
                     }
-                    if (small_n) {
-                        nm |= 1ull << n;
-                    } else {
-                        bool new_n = true;
-                        for (int j2 = 0; j2 < j && new_n; ++j2) {
-                            const int64_t v2 = __ldg(row + j2);
-                            new_n = !(v2 >= 0 && v2 < a.E && node_of[rank_of[v2]] == n);
-                        }
-                        if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
-                    }
+                    if (new_r) atomicAdd(&col_agg[a.E + r], 1);
+                    if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                 }
             }
-            tok_rmask[tl] = rm;
-            tok_nmask[tl] = nm;
         }
         // lane b of group g ends up with the warp's count for bit 32 g + b
         for (int g = 0; g < 2; ++g) {
@@ -360,66 +402,62 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int p = p_base + 32 * c;
-        if (p < npairs) {
+        if (c < cpw && p < npairs) {
             const int e = pe[c];
             a.pair_rank[pair0 + p] = e >= 0 ? col_excl[e] + my_base[e] + pr[c] : -1;
         }
     }
 
-    // (8) the last tile in ticket order holds the totals
+    // (8) the last tile in ticket order holds the totals. Each thread owns a
+    // contiguous run of experts: their counts, their sum (P) and, for the fused
+    // step 2, the exclusive prefix sum of the (padded) counts by a warp-shuffle scan
+    // of the runs and then of the warps' sums.
     if (tile == a.tiles - 1) {
-        int part = 0;
-        for (int c = tid; c < a.cols; c += kThreads) {
+        const int per = (a.E + kThreads - 1) / kThreads;
+        const int e0 = min(a.E, tid * per), e1 = min(a.E, e0 + per);
+        int part = 0, run = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int tot = col_excl[e] + col_agg[e];
+            a.per_expert[e] = tot;
+            a.ws_counts[e] = tot;
+            part += tot;
+            run += (tot + a.alignment - 1) / a.alignment * a.alignment;
+        }
+        for (int c = a.E + tid; c < a.cols; c += kThreads) {
             const int tot = col_excl[c] + col_agg[c];
-            if (c < a.E) {
-                a.per_expert[c] = tot;
-                a.ws_counts[c] = tot;
-                part += tot;
-            } else if (c < a.E + a.R) {
-                a.per_rank[c - a.E] = tot;
-            } else if (a.per_node) {
-                a.per_node[c - a.E - a.R] = tot;
-            }
+            if (c < a.E + a.R) a.per_rank[c - a.E] = tot;
+            else if (a.per_node) a.per_node[c - a.E - a.R] = tot;
+        }
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
         }
         part = warp_sum(part);
-        if (lane == 0) s_red[warp] = part;
-        __syncthreads();
-        if (tid == 0) {
-            int P = 0;
-            for (int w = 0; w < W; ++w) P += s_red[w];
-            a.hdr->total_pairs = P;
-            a.hdr->num_tokens = a.T;
-            a.hdr->num_topk = a.k;
+        if (lane == 31) {
+            s_red[warp] = incl;
+            s_red2[warp] = part;
         }
-        if (a.start_out) {
-            // step 2 fused: exclusive prefix sum of the (padded) counts over the experts.
-            // Each thread owns a contiguous run of experts; warp-shuffle scan of the
-            // runs' sums, then of the warps' sums.
-            const int per = (a.E + kThreads - 1) / kThreads;
-            const int e0 = tid * per, e1 = min(a.E, e0 + per);
-            int run = 0;
-            for (int e = e0; e < e1; ++e)
-                run += (col_excl[e] + col_agg[e] + a.alignment - 1) / a.alignment * a.alignment;
-            int incl = run;
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < W ? s_red[lane] : 0;
+            int wincl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
+                const int n = __shfl_up_sync(0xffffffffu, wincl, o);
+                if (lane >= o) wincl += n;
             }
-            __syncthreads();  // s_red is reused
-            if (lane == 31) s_red[warp] = incl;
-            __syncthreads();
-            if (warp == 0) {
-                const int v = lane < W ? s_red[lane] : 0;
-                int wincl = v;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int n = __shfl_up_sync(0xffffffffu, wincl, o);
-                    if (lane >= o) wincl += n;
-                }
-                if (lane < W) s_red[lane] = wincl - v;
-                if (lane == 31) *a.total_out = wincl;
+            const int P = warp_sum(lane < W ? s_red2[lane] : 0);
+            if (lane < W) s_red[lane] = wincl - v;
+            if (lane == 31) {
+                a.hdr->total_pairs = P;
+                a.hdr->num_tokens = a.T;
+                a.hdr->num_topk = a.k;
+                if (a.start_out) *a.total_out = wincl;
             }
+        }
+        if (a.start_out) {
             __syncthreads();
             int pos = s_red[warp] + incl - run;
             for (int e = e0; e < e1; ++e) {
