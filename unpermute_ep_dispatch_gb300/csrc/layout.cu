@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     int *col_excl = col_agg + a.cols_pad;  // [cols_pad] counts of earlier tiles
     int *rank_of = col_excl + a.cols_pad;  // [E] simulated rank of each expert
     int *node_of = rank_of + a.E;          // [R] simulated node of each rank
+    int16_t *s_pick = reinterpret_cast<int16_t *>(node_of + a.E);  // [tile pairs] expert or -1
     __shared__ int s_tile;
     __shared__ uint32_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
@@ -87,10 +88,6 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
-    }
-    for (int i = tid; i < a.tile_tokens; i += kThreads) {
-        tok_rmask[i] = 0;
-        tok_nmask[i] = 0;
     }
     for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
     for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
@@ -134,53 +131,11 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         pe[c] = (v >= 0 && v < a.E) ? (int)v : -1;
         if (v < -1 || v >= a.E) report(a.status, EPD_ERR_INVALID_EXPERT);
     }
-    // the ranks and nodes each token reaches, as bit masks when R, N <= 64 (a token
-    // counts once per rank and once per node), from the picks already in registers:
-    // a token's picks sit in consecutive lanes, so a segmented OR scan over the
-    // chunk leaves its mask in the segment's last lane, which merges it into shared
-    // memory (a token cut by a chunk boundary has two such lanes)
-    const bool small_r = a.R <= 64, small_n = a.N <= 64;
-    if ((small_r || small_n) && a.k > 0) {
-        const bool packed = a.R <= 32 && a.N <= 32;  // rank bits low, node bits high
+    // the picks, for the per-token rank and node masks of step (3)
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-            if (c >= live) break;
-            const int p = p_base + 32 * c;
-            const int e = pe[c];
-            const int tl = p / a.k;
-            const int first = max(0, lane - (p - tl * a.k));  // lane of the segment's first pick
-            unsigned long long rm = 0, nm = 0;
-            if (e >= 0) {
-                const int r = rank_of[e];
-                if (packed) {
-                    rm = (1ull << r) | (1ull << (32 + node_of[r]));
-                } else {
-                    if (small_r) rm = 1ull << r;
-                    if (small_n) nm = 1ull << node_of[r];
-                }
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long ur = __shfl_up_sync(0xffffffffu, rm, o);
-                if (lane - o >= first) rm |= ur;
-                if (!packed) {
-                    const unsigned long long un = __shfl_up_sync(0xffffffffu, nm, o);
-                    if (lane - o >= first) nm |= un;
-                }
-            }
-            const bool last = lane == 31 || (p + 1) % a.k == 0;
-            if (last && tl < ntok) {
-                if (packed) {
-                    if (rm) {
-                        atomicOr(&tok_rmask[tl], rm & 0xffffffffull);
-                        atomicOr(&tok_nmask[tl], rm >> 32);
-                    }
-                } else {
-                    if (rm) atomicOr(&tok_rmask[tl], rm);
-                    if (nm) atomicOr(&tok_nmask[tl], nm);
-                }
-            }
-        }
+    for (int c = 0; c < kChunks; ++c) {
+        const int p = p_base + 32 * c;
+        if (c < live && p < npairs) s_pick[p] = (int16_t)pe[c];
     }
     int *my_hist = hw + warp * hws;
 #pragma unroll
@@ -226,27 +181,30 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     }
 
     // (3) one lane per token, warps taken from the top so that they run beside the
-    // scan above: the tile's tokens per rank and per node from one ballot per mask
-    // bit; for R or N above 64 (no masks) each token counts its distinct ranks or
+    // scan above: the ranks and nodes the token reaches (read from its picks in
+    // shared memory), as bit masks when R, N <= 64 (a token counts once per rank and
+    // once per node), and the tile's tokens per rank and per node from one ballot
+    // per mask bit; for R or N above 64 each token counts its distinct ranks or
     // nodes by comparing its picks
+    const bool small_r = a.R <= 64, small_n = a.N <= 64;
     for (int base = (W - 1 - warp) * 32; base < ntok; base += kThreads) {
         const int tl = base + lane;
         unsigned long long rm = 0, nm = 0;
         if (tl < ntok) {
-            if (small_r) rm = tok_rmask[tl];
-            if (small_n) nm = tok_nmask[tl];
-            if (!small_r || !small_n) {
-                const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
-                for (int j = 0; j < a.k; ++j) {
-                    const int64_t v = __ldg(row + j);
-                    if (v < 0 || v >= a.E) continue;
-                    const int r = rank_of[v];
-                    const int n = node_of[r];
+            const int16_t *row = s_pick + tl * a.k;
+            for (int j = 0; j < a.k; ++j) {
+                const int e = row[j];
+                if (e < 0) continue;
+                const int r = rank_of[e];
+                const int n = node_of[r];
+                if (small_r) rm |= 1ull << r;
+                if (small_n) nm |= 1ull << n;
+                if (!small_r || !small_n) {
                     bool new_r = !small_r, new_n = !small_n;
                     for (int j2 = 0; j2 < j && (new_r || new_n); ++j2) {
-                        const int64_t v2 = __ldg(row + j2);
-                        if (v2 < 0 || v2 >= a.E) continue;
-                        const int r2 = rank_of[v2];
+                        const int e2 = row[j2];
+                        if (e2 < 0) continue;
+                        const int r2 = rank_of[e2];
                         if (r2 == r) new_r = false;
                         if (node_of[r2] == n) new_n = false;
                     }
@@ -254,6 +212,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
                     if (new_n) atomicAdd(&col_agg[a.E + a.R + n], 1);
                 }
             }
+            tok_rmask[tl] = rm;
+            tok_nmask[tl] = nm;
         }
         // lane b of group g ends up with the warp's count for bit 32 g + b
         for (int g = 0; g < 2; ++g) {
@@ -312,10 +272,10 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
                 if (small_r) {
                     hit = (tok_rmask[tl] >> r) & 1ull;
                 } else {
-                    const int64_t *row = a.topk + (pair0 + (int64_t)tl * a.k);
+                    const int16_t *row = s_pick + tl * a.k;
                     for (int j = 0; j < a.k && !hit; ++j) {
-                        const int64_t v = __ldg(row + j);
-                        hit = v >= 0 && v < a.E && rank_of[v] == r;
+                        const int e = row[j];
+                        hit = e >= 0 && rank_of[e] == r;
                     }
                 }
                 blk[i] = hit ? 1 : 0;
@@ -482,7 +442,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
 
 size_t layout_smem_bytes(int E, int cols_pad) {
     return 2 * (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
-           ((size_t)layout_warps(E) * (E + 1) + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int);
+           ((size_t)layout_warps(E) * (E + 1) + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int) +
+           (size_t)kLayoutTilePairs * sizeof(int16_t);
 }
 
 template <int W>
