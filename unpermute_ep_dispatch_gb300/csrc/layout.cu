@@ -9,21 +9,26 @@
 // One block per token tile (tile order from an atomic ticket, so a block only
 // ever waits on blocks that are already running). Inside a tile:
 //   * each warp walks a contiguous run of the tile's (token, pick) pairs in
-//     row-major order; lanes holding the same expert find each other with
-//     __match_any_sync, and the lowest of them adds the group's size to the
-//     warp's private shared-memory histogram (warp-aggregated, no atomics);
-//   * an exclusive scan across the warps' histograms gives each pair its rank
-//     among the tile's pairs of the same expert, in (t, j) order;
+//     row-major order; lanes holding the same expert find each other with one
+//     ballot per bit of the expert id, and the lowest of them adds the group's
+//     size to the warp's private shared-memory histogram (warp-aggregated, no
+//     atomics); the picks are parked in shared memory for the token masks;
+//   * an exclusive scan across the warps' histograms (one thread per expert)
+//     gives each pair its rank among the tile's pairs of the same expert, in
+//     (t, j) order; beside it, other warps build each token's rank and node bit
+//     masks and count the tile's tokens per rank and per node with ballots;
 //   * the tile's counts (experts, ranks, nodes) are published and the prefix
 //     over earlier tiles is read with a single-pass decoupled look-back: a
 //     warp polls the states of up to 32 earlier tiles at once and stops at the
 //     nearest one that has published its inclusive prefix;
 //   * prefix + warp base + rank inside the warp = the pair's rank inside its
 //     expert over the whole batch, stored in the workspace for ep_permute;
-//   * the tile that holds the last ticket writes the totals.
-// Every value is an integer sum, so the outputs are the same whichever order
-// the blocks run in. Waits are bounded: a wait that runs out sets
-// EPD_ERR_TIMEOUT and the block carries on.
+//   * the tile that holds the last ticket writes the totals (and, for
+//     ep_dispatch_layout_offsets, the expert offsets).
+// A call with a single tile takes no ticket and publishes nothing. Every value
+// is an integer sum, so the outputs are the same whichever order the blocks run
+// in. Waits are bounded: a wait that runs out sets EPD_ERR_TIMEOUT and the
+// block carries on.
 #include <atomic>
 #include <cstddef>
 
@@ -111,14 +116,14 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     const int npairs = ntok * a.k;
     const int64_t pair0 = (int64_t)t0 * a.k;
 
-    // (1) warp w owns a contiguous run of kChunks 32-pair chunks of the tile, in
-    // row-major order. All of a lane's picks are loaded at once, then each chunk
-    // is ranked: lanes holding the same expert find each other with one ballot per
+    // (1) warp w owns a contiguous run of cpw 32-pair chunks of the tile, in
+    // row-major order: pairs [32 cpw w, 32 cpw (w + 1)) (warp-major order, which the
+    // scan across warps relies on). A full tile has kChunks chunks per warp; a
+    // partial one spreads its pairs over all warps, and chunks past its last pair
+    // are skipped. All of a lane's picks are loaded at once, then each chunk is
+    // ranked: lanes holding the same expert find each other with one ballot per
     // bit of the expert id, and the lowest of them adds the group's size to the
     // warp's private histogram.
-    // A partial tile spreads its pairs over all warps: cpw chunks per warp, warp w
-    // owning pairs [32 cpw w, 32 cpw (w + 1)) (pairs stay in warp-major order, which
-    // the scan across warps relies on); chunks past the tile's last pair are skipped.
     int pe[kChunks], pr[kChunks];
     const int cpw = max(1, min(kChunks, (npairs + kThreads - 1) / kThreads));
     const int p_base = warp * 32 * cpw + lane;
