@@ -482,6 +482,38 @@ def test_lowlatency_edges(T, H):
     _ll_compare(case, rows=max(T, 1))
 
 
+def test_lowlatency_half_view():
+    """A view of half the experts loads rows before their slots are known."""
+    case = _bf16_decode_case(T=300, seed=3006)
+    _ll_compare(case, rows=300, b=128, e_end=256)
+
+
+@pytest.mark.parametrize("T", [0, 5, 130])
+def test_lowlatency_zero_topk(T):
+    case = workloads.make_random_case(T=T, H=256, k=0, E=16, R=8, N=2, dtype="bf16", seed=T,
+                                      routing="uniform", experts="random")
+    _ll_compare(case, rows=4)
+
+
+def test_lowlatency_rejects_workspace_of_another_layout():
+    """A workspace whose header names another T: EPD_ERR_INVALID_ARG and no output
+    written (each warp checks the header before its first store)."""
+    dev = torch.device("cuda")
+    a = _bf16_decode_case(T=64, seed=3007)
+    b = _bf16_decode_case(T=96, seed=3008)
+    ws = epd.new_workspace(b.T, b.k, b.E, b.R, b.N, dev)
+    st = epd.new_status(dev)
+    epd.ep_dispatch_layout(a.topk_idx.to(dev), a.E, a.R, a.N, ws, st)
+    torch.cuda.synchronize()
+    oi = torch.full((b.T, b.k), 123, dtype=torch.int32, device=dev)
+    rc = torch.full((b.E,), 77, dtype=torch.int32, device=dev)
+    epd.ep_permute_lowlatency(b.x.to(dev), b.topk_idx.to(dev), b.E, 16, ws, st,
+                              output_index=oi, recv_count=rc)
+    torch.cuda.synchronize()
+    assert int(st.item()) == epd.EPD_ERR_INVALID_ARG
+    assert torch.all(oi == 123) and torch.all(rc == 77)
+
+
 def test_lowlatency_prefill_size():
     case = _bf16_decode_case(T=2048, seed=3004)
     _ll_compare(case, rows=256)

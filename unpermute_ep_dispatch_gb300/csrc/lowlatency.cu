@@ -15,7 +15,10 @@
 // half-warp owns one block: 16-byte bf16 loads, the block's absolute maximum by
 // half-warp shuffles, scale = amax / 448 and q = e4m3(x / scale) with IEEE
 // divisions and the saturating round-to-nearest-even conversion, then 8-byte
-// stores of the quantised block to each row the token goes to.
+// stores of the quantised block to each row the token goes to. Each warp checks
+// the workspace header itself and issues the loads that do not depend on a slot
+// (the header, the picks and their ranks, and over wide views the row) before its
+// first store.
 #include <cuda_fp8.h>
 
 #include "epd_common.cuh"
@@ -50,20 +53,14 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 
 __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
     __shared__ int s_row[kWarps][EPD_MAX_TOPK];
-    __shared__ int s_ok;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();  // pair ranks and counts come from the layout kernel
-    if (threadIdx.x == 0) {
-        s_ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
-        if (!s_ok && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
-    }
-    __syncthreads();
-    if (!s_ok) return;
-    if (blockIdx.x == 0)
-        for (int e = threadIdx.x; e < a.e_end - a.e_begin; e += kThreads) {
-            const int64_t c = a.counts[a.e_begin + e];
-            a.recv_count[e] = (int32_t)(c < a.rows ? c : a.rows);
-        }
+    // Each warp checks the workspace header itself, and every load that does not
+    // depend on a slot (the header, the row, the picks and their ranks) is issued
+    // before the first store, which waits for the header's verdict.
+    int hdr_ok = 0;
+    if (lane == 0) hdr_ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
+    bool checked = false;
 
     const int C = a.H >> 7;                // 128-column blocks per row
     const int upt = (C + 1) >> 1;          // units (block pairs) per token
@@ -72,21 +69,53 @@ __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
     const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
     const int64_t u_end = units * (gw + 1) / nw;
     const int half = lane >> 4, hl = lane & 15;
+    // rows are loaded before their slots are known over views of at least a quarter
+    // of the experts (nearly every token is copied); a narrow view copies few tokens
+    // and loads a row only once it has a slot
+    const bool early = a.k > 0 && 4 * (a.e_end - a.e_begin) >= a.E;
     int cur_t = -1;
     bool any = false;
     for (int64_t u = units * gw / nw; u < u_end; ++u) {
         const int t = (int)(u / upt);
         const int ch = (int)(u - (int64_t)t * upt);
+        const int c = 2 * ch + half;       // this half-warp's block
+        const bool active = c < C;
+        const uint8_t *src = a.x + ((int64_t)t * a.H + 128 * c + 8 * hl) * 2;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (active && early) raw = ld_stream16(src);
         if (t != cur_t) {
             cur_t = t;
+            int64_t pe[2];
+            int32_t pr[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {  // k <= 64: at most two picks per lane
+                const int j = lane + 32 * q;
+                pe[q] = -1;
+                pr[q] = -1;
+                if (j < a.k) {
+                    const int64_t idx = (int64_t)t * a.k + j;
+                    pe[q] = a.topk[idx];
+                    pr[q] = a.pair_rank[idx];
+                }
+            }
+            if (!checked) {
+                checked = true;
+                if (!__shfl_sync(0xffffffffu, hdr_ok, 0)) {
+                    if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, EPD_ERR_INVALID_ARG);
+                    return;
+                }
+            }
             int has = 0;
             __syncwarp();
-            for (int j = lane; j < a.k; j += 32) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int j = lane + 32 * q;
+                if (j >= a.k) continue;
                 const int64_t idx = (int64_t)t * a.k + j;
-                const int64_t e = a.topk[idx];
+                const int64_t e = pe[q];
                 int row = -1;
                 if (e >= a.e_begin && e < a.e_end) {
-                    const int64_t r = a.pair_rank[idx];
+                    const int64_t r = pr[q];
                     if (r >= 0 && r < a.rows) {
                         row = (int)((e - a.e_begin) * a.rows + r);
                         if (ch == 0 && a.src_token) a.src_token[row] = t;
@@ -102,12 +131,10 @@ __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
             __syncwarp();
         }
         if (!any) continue;
-        const int c = 2 * ch + half;       // this half-warp's block
-        const bool active = c < C;
+        if (active && !early) raw = ld_stream16(src);
         float v[8];
         float amax = 0.0f;
         if (active) {
-            const uint4 raw = ld_stream16(a.x + ((int64_t)t * a.H + 128 * c + 8 * hl) * 2);
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -136,6 +163,12 @@ __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
             }
         }
     }
+    // recv_count by block 0 (after its warps' units: off the path of the rows)
+    if (blockIdx.x == 0 && __shfl_sync(0xffffffffu, hdr_ok, 0))
+        for (int e = threadIdx.x; e < a.e_end - a.e_begin; e += kThreads) {
+            const int64_t c = a.counts[a.e_begin + e];
+            a.recv_count[e] = (int32_t)(c < a.rows ? c : a.rows);
+        }
     pdl_trigger();
 }
 
