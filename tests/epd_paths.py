@@ -43,10 +43,12 @@ def oracle_path(case, capacity=None, topk_override=None, alignment=1):
 class GpuPath:
     """Device-resident buffers for one case and the four C ABI calls on them."""
 
-    def __init__(self, case, device="cuda", capacity=None, stream=None, alignment=1):
+    def __init__(self, case, device="cuda", capacity=None, stream=None, alignment=1,
+                 fused=False):
         self.case = case
         self.dev = torch.device(device)
         self.alignment = alignment
+        self.fused = fused  # step() runs ep_dispatch_layout_offsets instead of layout + scan
         self.cap = default_capacity(case, alignment) if capacity is None else int(capacity)
         self.stream = stream
         d = self.dev
@@ -104,9 +106,20 @@ class GpuPath:
         epd.ep_unpermute(eo, self.output_index, self.w, self.status, y=self.y,
                          stream=self.stream)
 
+    def layout_offsets(self):
+        c = self.case
+        epd.ep_dispatch_layout_offsets(self.topk, c.E, c.R, c.N, self.ws, self.status,
+                                       alignment=self.alignment, tokens_per_expert=self.per_e,
+                                       tokens_per_rank=self.per_r, tokens_per_rdma_rank=self.per_n,
+                                       is_token_in_rank=self.itr, expert_start_loc=self.start,
+                                       total_rows=self.total, stream=self.stream)
+
     def step(self):
-        self.layout()
-        self.scan()
+        if self.fused:
+            self.layout_offsets()
+        else:
+            self.layout()
+            self.scan()
         self.permute()
         self.unpermute()
 

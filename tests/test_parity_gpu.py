@@ -560,3 +560,50 @@ def test_fused_layout_offsets_match_separate_steps(name, T, alignment):
     g.permute()
     g.unpermute()
     compare(g.results(), oracle_path(case, alignment=alignment))
+
+
+# ----------------------------------------------------------------------------- seeded random sweep
+_TOPOS = [(1, 1, 1), (2, 2, 1), (4, 2, 2), (16, 8, 2), (64, 8, 1), (96, 12, 3), (256, 32, 4),
+          (512, 64, 8), (1024, 128, 16), (4096, 512, 8)]
+
+
+def _sweep_config(i):
+    """Configuration i of the sweep, drawn from its own seed: topology, k (0 and 64
+    included), T across tile boundaries, dtype and row width, routing style, dropped
+    picks, alignment and whether the offsets are fused into the layout launch. Rows
+    are kept to a few MB so that the oracle finishes in well under a second."""
+    rng = np.random.default_rng(9000 + i)
+    E, R, N = _TOPOS[int(rng.integers(len(_TOPOS)))]
+    k = int(rng.choice([0, 1, 2, 3, 4, 6, 8, 9, 16, 64]))
+    T = int(rng.choice([0, 1, 7, 31, 32, 33, 100, 257, 1000, 2049, 4097]))
+    if k == 64:
+        T = min(T, 300)
+    dtype = str(rng.choice(["bf16", "fp8"]))
+    widths = [128, 256, 384] if dtype == "fp8" else [8, 64, 136, 1024]
+    elem = 1 if dtype == "fp8" else 2
+    widths = [h for h in widths if T * max(k, 1) * h * elem <= 8 << 20] or widths[:1]
+    H = int(rng.choice(widths))
+    routing = str(rng.choice(["uniform", "repeats", "zipf", "invalid"]))
+    if routing == "uniform" and k > E:
+        routing = "repeats"
+    if routing == "zipf" and (E < 256 or k > 16):
+        routing = "repeats"
+    p_invalid = float(rng.choice([0.0, 0.1, 0.5]))
+    alignment = int(rng.choice([1, 1, 4, 64, 128]))
+    fused = bool(rng.integers(2))
+    return dict(E=E, R=R, N=N, k=k, T=T, dtype=dtype, H=H, routing=routing,
+                p_invalid=p_invalid, alignment=alignment, fused=fused)
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_sweep(i):
+    cfg = _sweep_config(i)
+    case = workloads.make_random_case(T=cfg["T"], H=cfg["H"], k=cfg["k"], E=cfg["E"],
+                                      R=cfg["R"], N=cfg["N"], dtype=cfg["dtype"], seed=9100 + i,
+                                      routing=cfg["routing"], p_invalid=cfg["p_invalid"],
+                                      experts="random", zero_experts=20)
+    g = GpuPath(case, alignment=cfg["alignment"], fused=cfg["fused"])
+    g.step()
+    got = g.results()
+    want = oracle_path(case, alignment=cfg["alignment"])
+    compare(got, want)
