@@ -607,3 +607,94 @@ def test_random_sweep(i):
     got = g.results()
     want = oracle_path(case, alignment=cfg["alignment"])
     compare(got, want)
+
+
+def _sweep_view(rng, E, R):
+    kind = str(rng.choice(["whole", "half", "rank", "quarter"]))
+    if kind == "whole":
+        return 0, E
+    if kind == "half":
+        return (0, E // 2) if E >= 2 and rng.integers(2) else (E - max(1, E // 2), E)
+    if kind == "quarter":
+        q = max(1, E // 4)
+        b = int(rng.integers(0, E - q + 1))
+        return b, b + q
+    r = int(rng.integers(R))
+    return r * (E // R), (r + 1) * (E // R)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_sweep_permute_ex(i):
+    """ep_permute_ex over random views, scale word counts and layouts (row- or
+    column-major, leading dimension with slack) and alignments, against the oracle."""
+    import oracle
+    rng = np.random.default_rng(9500 + i)
+    E, R, N = _TOPOS[int(rng.integers(3, 8))]
+    k = int(rng.choice([1, 2, 6, 8]))
+    T = int(rng.choice([1, 33, 257, 1000, 2049]))
+    alignment = int(rng.choice([1, 4, 128]))
+    scales = str(rng.choice(["f32", "ue8m0", "words"]))
+    H = int(rng.choice([128, 256, 1024]))
+    case = workloads.make_random_case(T=T, H=H, k=k, E=E, R=R, N=N, dtype="fp8", seed=9600 + i,
+                                      routing="repeats", p_invalid=0.2, experts="random",
+                                      scales="ue8m0" if scales == "ue8m0" else "f32")
+    if scales == "words":  # opaque 32-bit words, more than 16 per row
+        words = torch.randint(-2**31, 2**31 - 1, (T, int(rng.choice([17, 40]))),
+                              generator=torch.Generator().manual_seed(i), dtype=torch.int32)
+    else:
+        words = case.x_scale.contiguous()
+        if words.dtype == torch.float32:
+            words = words.view(torch.int32)
+    g = GpuPath(case, alignment=alignment, fused=True)
+    g.layout_offsets()
+    torch.cuda.synchronize()
+    b, e = _sweep_view(rng, E, R)
+    cap = oracle.aligned_capacity(T, k, E, alignment) if alignment > 1 else T * k
+    col = bool(rng.integers(2))
+    ld = cap + int(rng.integers(0, 40)) if col else None
+    ostart = g.start.cpu().numpy()
+    out, osc, mi, oi = epd.ep_permute_ex(g.x, words.to(g.dev), g.topk, E, g.start, g.ws, g.status,
+                                         capacity_rows=cap, expert_begin=b, expert_end=e,
+                                         scale_col_major=col, scale_ld=ld)
+    torch.cuda.synchronize()
+    assert int(g.status.item()) == 0
+    lay = oracle.dispatch_layout(case.topk_idx.numpy(), E, R, N)
+    if alignment == 1:
+        want_start, _ = oracle.scan_offsets(lay["tokens_per_expert"])
+    else:
+        want_start, _ = oracle.scan_offsets_aligned(lay["tokens_per_expert"], alignment)
+    assert np.array_equal(ostart, want_start)
+    want = oracle.permute_ex(row_bytes(case.x), _words(words), case.topk_idx.numpy(), E,
+                             want_start, cap, expert_begin=b, expert_end=e,
+                             scale_col_major=col, scale_ld=ld)
+    got_oi = oi.cpu().numpy()
+    assert np.array_equal(got_oi, want["output_index"])
+    assert np.array_equal(mi.cpu().numpy(), want["m_indices"])
+    rows = got_oi[got_oi >= 0]
+    assert np.array_equal(row_bytes(out)[rows], want["out"][rows])
+    gs = _words(osc)
+    if col:
+        assert np.array_equal(gs[:, rows], want["out_scale"][:, rows])
+    else:
+        assert np.array_equal(gs[rows], want["out_scale"][rows])
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_sweep_lowlatency(i):
+    """ep_permute_lowlatency over random sizes, views and rectangle heights (some
+    too small, which must report EPD_ERR_CAPACITY and drop exactly the oracle's
+    picks), against the oracle."""
+    import oracle
+    rng = np.random.default_rng(9700 + i)
+    E, R, N = _TOPOS[int(rng.integers(3, 8))]
+    k = int(rng.choice([1, 2, 4, 8]))
+    T = int(rng.choice([1, 31, 128, 300, 1000]))
+    H = int(rng.choice([128, 384, 1024]))
+    case = workloads.make_random_case(T=T, H=H, k=k, E=E, R=R, N=N, dtype="bf16",
+                                      seed=9800 + i, routing="repeats", p_invalid=0.1,
+                                      experts="random")
+    b, e = _sweep_view(rng, E, R)
+    rows = int(rng.choice([1, 4, max(1, T * k // max(E, 1)), T]))
+    want = oracle.permute_lowlatency(bits16(case.x), case.topk_idx.numpy(), E, rows, b, e)
+    _ll_compare(case, rows=rows, b=b, e_end=e,
+                expect_status=epd.EPD_ERR_CAPACITY if want["overflow"] else 0)
