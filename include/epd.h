@@ -219,6 +219,29 @@ EPD_API epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float *x
                         int32_t *output_index, int32_t *status, epd_stream_t stream);
 
 /*
+ * Steps 1 to 3 in one call: the dispatch layout with its (aligned) offsets, then
+ * the permute over the whole expert range with row-major scales -- exactly the
+ * outputs of ep_dispatch_layout_offsets followed by ep_permute on the same
+ * arguments, workspace state included. A small batch (T*k <= 4096, T <= 1024,
+ * E <= 1024, R and N <= 64; a decode step) runs as one kernel in which every
+ * block counts and scans the whole batch's picks itself and copies its own
+ * tokens' rows; larger batches run the two kernels. Arguments, layouts and errors
+ * as in those two calls; tokens_per_rdma_rank and is_token_in_rank may be NULL.
+ * capacity_rows must hold the (aligned) total (a slot outside sets
+ * EPD_ERR_CAPACITY). The pages have no single call for these steps (DeepEP
+ * computes the layout in get_dispatch_layout before dispatch).
+ */
+EPD_API epd_status_t ep_dispatch(const void *x, epd_dtype_t dtype, const float *x_scale,
+                                 const int64_t *topk_idx, int num_tokens, int num_topk,
+                                 int hidden, int num_experts, int num_ranks, int num_rdma_ranks,
+                                 int alignment, int32_t *tokens_per_expert,
+                                 int32_t *tokens_per_rank, int32_t *tokens_per_rdma_rank,
+                                 uint8_t *is_token_in_rank, int32_t *expert_start_loc,
+                                 int32_t *total_rows, void *workspace, int64_t capacity_rows,
+                                 void *out, float *out_scale, int32_t *m_indices,
+                                 int32_t *output_index, int32_t *status, epd_stream_t stream);
+
+/*
  * Output options of ep_permute_ex.
  *   expert_begin, expert_end: the view -- only pairs whose expert is in
  *     [expert_begin, expert_end) are placed (0 and num_experts for all

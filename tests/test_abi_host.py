@@ -162,3 +162,33 @@ def test_permute_ex_rejects_bad_views(lib):
     assert call(V(0, 8, 3, 0, 0)) == E                           # scales without pointers
     assert call(V(0, 8, 0, 0, 0), row_bytes=60) == E             # rows not 16-byte multiples
     assert call(V(0, 8, 0, 0, 0), cap=-1) == E
+
+
+def test_dispatch_rejects_bad_args(lib):
+    E = _binding.EPD_ERR_INVALID_ARG
+    f = lib.ep_dispatch
+    ok = dict(x=FAKE, dt=0, xs=NULL, topk=FAKE, T=4, k=2, H=64, E=8, R=4, N=2, align=1,
+              per_e=FAKE, per_r=FAKE, per_n=NULL, itr=NULL, start=FAKE, total=FAKE, ws=FAKE,
+              cap=8, out=FAKE, outs=NULL, mi=FAKE, oi=FAKE, st=FAKE, s=NULL)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(*a.values())
+    assert call(cap=7) == E                      # capacity below T*k
+    assert call(cap=1 << 40) == E                # beyond int32 rows
+    assert call(H=60) == E                       # bf16 rows need H % 8
+    assert call(xs=FAKE) == E                    # bf16 takes no scales
+    assert call(dt=1, H=64, xs=FAKE, outs=FAKE) == E   # fp8 needs H % 128
+    assert call(dt=1, H=128) == E                # fp8 without scales
+    assert call(dt=7) == E                       # unknown dtype
+    assert call(R=3) == E                        # E % R
+    assert call(N=3) == E                        # R % N
+    assert call(align=0) == E
+    assert call(align=8192) == E                 # above EPD_MAX_ALIGNMENT
+    assert call(x=FAKE_ODD) == E                 # rows must be 16-byte aligned
+    assert call(out=FAKE_ODD) == E
+    assert call(ws=NULL) == E
+    assert call(st=NULL) == E
+    assert call(start=NULL) == E
+    assert call(total=NULL) == E
+    assert call(mi=NULL) == E

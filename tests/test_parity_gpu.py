@@ -698,3 +698,91 @@ def test_random_sweep_lowlatency(i):
     want = oracle.permute_lowlatency(bits16(case.x), case.topk_idx.numpy(), E, rows, b, e)
     _ll_compare(case, rows=rows, b=b, e_end=e,
                 expect_status=epd.EPD_ERR_CAPACITY if want["overflow"] else 0)
+
+
+# ----------------------------------------------------------------------------- ep_dispatch
+def _dispatch_path(case, alignment=1, capacity=None):
+    """ep_dispatch then ep_unpermute; results in the GpuPath.results() form."""
+    g = GpuPath(case, alignment=alignment, capacity=capacity)
+    r = epd.ep_dispatch(g.x, g.xs, g.topk, case.E, case.R, case.N, g.ws, g.status,
+                        alignment=alignment, capacity_rows=g.cap, tokens_per_expert=g.per_e,
+                        tokens_per_rank=g.per_r, tokens_per_rdma_rank=g.per_n,
+                        is_token_in_rank=g.itr, expert_start_loc=g.start, total_rows=g.total,
+                        out=g.out, out_scale=g.out_scale, m_indices=g.m_indices,
+                        output_index=g.output_index)
+    assert r["out"] is g.out
+    g.unpermute()
+    return g
+
+
+DISPATCH_CASES = [
+    # (name, T, H, k, E, R, N, dtype, routing, p_invalid, alignment)
+    ("decode", 128, 7168, 8, 256, 32, 4, "fp8", "uniform", 0.0, 1),
+    ("decode_aligned", 128, 7168, 8, 256, 32, 4, "fp8", "uniform", 0.0, 128),
+    ("tiny", 64, 256, 2, 16, 8, 2, "bf16", "uniform", 0.0, 1),
+    ("prefill_small", 500, 4096, 6, 64, 8, 1, "bf16", "repeats", 0.02, 1),
+    ("k1_many_tokens", 1024, 136, 1, 16, 4, 2, "bf16", "repeats", 0.1, 4),
+    ("k4_4096_pairs", 1024, 128, 4, 1024, 64, 64, "fp8", "repeats", 0.2, 1),
+    ("k64", 40, 64, 64, 4, 2, 1, "bf16", "repeats", 0.1, 1),
+    ("k0", 77, 64, 0, 16, 8, 2, "bf16", "uniform", 0.0, 1),
+    ("T0", 0, 64, 8, 16, 8, 2, "bf16", "uniform", 0.0, 1),
+    ("all_dropped", 50, 64, 4, 16, 8, 2, "bf16", "repeats", 1.0, 64),
+    ("scale_words_past_threads", 1000, 9216, 4, 64, 8, 2, "fp8", "uniform", 0.0, 1),
+    ("block_rows_64KiB", 1000, 8192, 4, 64, 8, 2, "bf16", "uniform", 0.0, 1),
+    ("two_kernels_dsv3", 2048, 7168, 8, 256, 32, 4, "fp8", "uniform", 0.0, 1),
+    ("two_kernels_many_experts", 300, 64, 8, 4096, 512, 8, "bf16", "uniform", 0.0, 1),
+    ("two_kernels_wide_ranks", 200, 64, 8, 256, 128, 4, "bf16", "uniform", 0.0, 1),
+]
+
+
+@pytest.mark.parametrize("cfg", DISPATCH_CASES, ids=[c[0] for c in DISPATCH_CASES])
+def test_dispatch_matches_oracle(cfg):
+    """ep_dispatch (one kernel for a small batch, the two kernels beyond) gives the
+    oracle's counts, masks, offsets, rows, scales, m_indices and output_index."""
+    _, T, H, k, E, R, N, dtype, routing, p_invalid, alignment = cfg
+    case = workloads.make_random_case(T=T, H=H, k=k, E=E, R=R, N=N, dtype=dtype,
+                                      seed=T * 13 + k + E, routing=routing,
+                                      p_invalid=p_invalid, experts="random")
+    g = _dispatch_path(case, alignment=alignment)
+    compare(g.results(), oracle_path(case, alignment=alignment))
+
+
+@pytest.mark.parametrize("T", [1, 128, 700])
+def test_dispatch_equals_separate_calls_and_workspace(T):
+    """Same bytes as ep_dispatch_layout_offsets + ep_permute, workspace pair ranks and
+    header included (a later ep_permute on the workspace gives the same rows)."""
+    case = workloads.make_random_case(T=T, H=256, k=8, E=256, R=32, N=4, dtype="fp8",
+                                      seed=T, routing="uniform", experts="random")
+    a = _dispatch_path(case)
+    b = GpuPath(case, fused=True)
+    b.step()
+    ra, rb = a.results(), b.results()
+    for key in ("tokens_per_expert", "tokens_per_rank", "tokens_per_rdma_rank",
+                "is_token_in_rank", "expert_start_loc", "m_indices", "output_index"):
+        assert np.array_equal(ra[key], rb[key]), key
+    n = T * 8 * 4
+    off = 256  # per-pair ranks follow the 256-byte header block
+    assert torch.equal(a.ws[off:off + n], b.ws[off:off + n])
+    # the header names this layout: ep_permute on a's workspace succeeds and agrees
+    out, _, mi, oi = epd.ep_permute(a.x, a.xs, a.topk, case.E, a.start, a.ws, a.status)
+    torch.cuda.synchronize()
+    assert int(a.status.item()) == 0
+    assert np.array_equal(oi.cpu().numpy(), rb["output_index"])
+    assert np.array_equal(mi.cpu().numpy(), rb["m_indices"])
+
+
+def test_dispatch_reports_invalid_ids_and_capacity():
+    case = workloads.make_random_case(T=100, H=64, k=4, E=16, R=8, N=2, dtype="bf16", seed=5,
+                                      routing="uniform", experts="random")
+    bad = case.topk_idx.clone()
+    bad[7, 2] = 16
+    bad[90, 0] = -3
+    case_bad = workloads.Case(**{**case.__dict__, "topk_idx": bad})
+    g = _dispatch_path(case_bad)
+    got = g.results()
+    assert got["status"] == epd.EPD_ERR_INVALID_EXPERT
+    clean = torch.where((bad >= -1) & (bad < 16), bad, torch.full_like(bad, -1))
+    compare(got, oracle_path(case, topk_override=clean), check_status=False)
+    # aligned offsets with a buffer of only T*k rows: slots past it are reported
+    g2 = _dispatch_path(case, alignment=64, capacity=100 * 4)
+    assert g2.results()["status"] == epd.EPD_ERR_CAPACITY

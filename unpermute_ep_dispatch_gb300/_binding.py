@@ -53,6 +53,8 @@ SIGNATURES = {
     "ep_scan_offsets": (_I, [_P, _I, _P, _P, _P, _P]),
     "ep_scan_offsets_aligned": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "ep_permute": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
+    "ep_dispatch": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                         _I64, _P, _P, _P, _P, _P, _P]),
     "ep_permute_ex": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _I64, ctypes.POINTER(PermuteView),
                            _P, _P, _P, _P, _P, _P]),
     "ep_unpermute": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _P]),
@@ -326,6 +328,71 @@ def ep_permute(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: torch
                                    _ptr(output_index), _ptr(status), _stream(stream, dev))
     _check(rc, "ep_permute")
     return out, out_scale, m_indices, output_index
+
+
+def ep_dispatch(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: torch.Tensor,
+                num_experts: int, num_ranks: int, num_rdma_ranks: int, workspace: torch.Tensor,
+                status: torch.Tensor, alignment: int = 1, capacity_rows: Optional[int] = None,
+                tokens_per_expert=None, tokens_per_rank=None, tokens_per_rdma_rank=None,
+                is_token_in_rank=None, expert_start_loc=None, total_rows=None, out=None,
+                out_scale=None, m_indices=None, output_index=None,
+                with_rdma: Optional[bool] = None, with_is_token_in_rank: bool = True,
+                stream=None):
+    """Steps 1 to 3 in one call (layout, offsets, permute; see epd.h). x: [T, H]
+    bfloat16, or float8_e4m3fn with x_scale [T, H/128] float32. Returns a dict with
+    tokens_per_rank, tokens_per_rdma_rank (or None), tokens_per_expert,
+    is_token_in_rank (or None), expert_start_loc, total_rows, out, out_scale (or
+    None), m_indices and output_index."""
+    if x.dtype == torch.bfloat16:
+        dt = EPD_BF16
+        if x_scale is not None:
+            raise ValueError("bf16 rows take no scales")
+    elif x.dtype == torch.float8_e4m3fn:
+        dt = EPD_FP8_E4M3
+        if x_scale is None:
+            raise ValueError("fp8 rows need x_scale [T, H/128] float32")
+    else:
+        raise ValueError(f"x must be bfloat16 or float8_e4m3fn, got {x.dtype}")
+    _want(x, "x", x.dtype)
+    dev = x.device
+    T, H = x.shape
+    _want(topk_idx, "topk_idx", torch.int64, device=dev)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, k] with the T of x")
+    k = topk_idx.shape[1]
+    E, R, N = int(num_experts), int(num_ranks), int(num_rdma_ranks)
+    M = T * k if capacity_rows is None else int(capacity_rows)
+    _want(workspace, "workspace", torch.uint8, device=dev)
+    _want(status, "status", torch.int32, (1,), dev)
+    if workspace.numel() < epd_workspace_bytes(T, k, E, R, N):
+        raise ValueError("workspace too small for this layout")
+    if with_rdma is None:
+        with_rdma = N > 1 or tokens_per_rdma_rank is not None
+    per_e = _out(tokens_per_expert, "tokens_per_expert", torch.int32, (E,), dev)
+    per_r = _out(tokens_per_rank, "tokens_per_rank", torch.int32, (R,), dev)
+    per_n = _out(tokens_per_rdma_rank, "tokens_per_rdma_rank", torch.int32, (N,), dev) \
+        if with_rdma else None
+    itr = _out(is_token_in_rank, "is_token_in_rank", torch.bool, (T, R), dev) \
+        if with_is_token_in_rank else None
+    start = _out(expert_start_loc, "expert_start_loc", torch.int32, (E,), dev)
+    total = _out(total_rows, "total_rows", torch.int32, (1,), dev)
+    out = _out(out, "out", x.dtype, (M, H), dev)
+    if dt == EPD_FP8_E4M3:
+        _want(x_scale, "x_scale", torch.float32, (T, H // 128), dev)
+        out_scale = _out(out_scale, "out_scale", torch.float32, (M, H // 128), dev)
+    else:
+        out_scale = None
+    m_indices = _out(m_indices, "m_indices", torch.int32, (M,), dev)
+    output_index = _out(output_index, "output_index", torch.int32, (T, k), dev)
+    rc = load_library().ep_dispatch(
+        _ptr(x), dt, _ptr(x_scale), _ptr(topk_idx), T, k, H, E, R, N, int(alignment),
+        _ptr(per_e), _ptr(per_r), _ptr(per_n), _ptr(itr), _ptr(start), _ptr(total),
+        _ptr(workspace), M, _ptr(out), _ptr(out_scale), _ptr(m_indices), _ptr(output_index),
+        _ptr(status), _stream(stream, dev))
+    _check(rc, "ep_dispatch")
+    return dict(tokens_per_rank=per_r, tokens_per_rdma_rank=per_n, tokens_per_expert=per_e,
+                is_token_in_rank=itr, expert_start_loc=start, total_rows=total, out=out,
+                out_scale=out_scale, m_indices=m_indices, output_index=output_index)
 
 
 def ep_permute_ex(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_idx: torch.Tensor,

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "libepd")
 LIB = os.path.join(PKG, "libepd.so")
-SOURCES = ["layout.cu", "scan.cu", "permute.cu", "unpermute.cu", "lowlatency.cu"]
+SOURCES = ["layout.cu", "scan.cu", "permute.cu", "unpermute.cu", "lowlatency.cu", "dispatch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
