@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     __shared__ uint8_t s_rank_of[kSmallExperts], s_node_of[64];
     __shared__ int s_rank[kSmallBlockPairs], s_slot[kSmallBlockPairs];
     __shared__ int s_wsum[kWarps], s_wpairs[kWarps];
-    __shared__ int s_total, s_pairs, s_rows_ok;
+    __shared__ int s_total, s_pairs;
+    __shared__ bool s_rows_ok;
     __shared__ int s_col[kSmallCols];  // this block's tallies of tokens per rank / node
     __shared__ __align__(8) uint64_t s_bar;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -217,24 +218,27 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     // is_token_in_rank rows, and tally the batch's tokens for this block's share of
     // the rank and node columns.
     const int cols = a.R + (a.per_node ? a.N : 0);
+    bool issued = false;  // this lane of warp 0 has bulk stores in flight
     if (warp == 0) {
-        if (lane == 0) {
-            s_rows_ok = 1;
-            if (copy) {
-                if (mbar_wait_bounded(&s_bar, 0u, kWaitLimit)) {
-                    fence_proxy_async_smem();
-                    for (int tl = 0; tl < nt; ++tl)
-                        for (int j = 0; j < a.k; ++j) {
-                            const int s = s_slot[tl * a.k + j];
-                            if (s >= 0)
-                                bulk_store(a.out + (int64_t)s * a.row_bytes, s_rows + tl * stride,
-                                           (uint32_t)a.row_bytes);
-                        }
-                    bulk_commit();
-                } else {
-                    report(a.status, EPD_ERR_TIMEOUT);
-                    s_rows_ok = 0;
+        bool landed = true;
+        if (copy) {
+            if (lane == 0) landed = mbar_wait_bounded(&s_bar, 0u, kWaitLimit);
+            landed = __shfl_sync(0xffffffffu, landed, 0);
+            if (lane == 0) {
+                s_rows_ok = landed;
+                if (!landed) report(a.status, EPD_ERR_TIMEOUT);
+            }
+            if (landed) {
+                // lane i issues the stores of (token, pick) pairs i, i + 32, ...
+                fence_proxy_async_smem();
+                for (int q = lane; q < q_end; q += 32) {
+                    const int s = s_slot[q];
+                    if (s < 0) continue;
+                    bulk_store(a.out + (int64_t)s * a.row_bytes, s_rows + (q / a.k) * stride,
+                               (uint32_t)a.row_bytes);
+                    issued = true;
                 }
+                if (issued) bulk_commit();
             }
         }
     } else {
@@ -317,10 +321,8 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     }
     // the bulk stores read shared memory until they complete; loads that outlived a
     // wait that gave up land before the block's shared memory is released
-    if (tid == 0 && copy) {
-        if (s_rows_ok) bulk_wait_all();
-        else mbar_wait_bounded(&s_bar, 0u, kWaitLimit);
-    }
+    if (issued) bulk_wait_all();
+    if (tid == 0 && copy && !s_rows_ok) mbar_wait_bounded(&s_bar, 0u, kWaitLimit);
     pdl_trigger();
 }
 
