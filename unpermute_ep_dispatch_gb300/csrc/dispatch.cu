@@ -119,10 +119,11 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
             bulk_load(s_rows + tl * stride, a.x + (int64_t)(t_begin + tl) * a.row_bytes,
                       (uint32_t)a.row_bytes, &s_bar);
     }
-    // and their scale words, into the registers of warps 1.. (which store them)
+    // and their scale words, into the registers of warps 1 and 2 (which store them)
     const int nsc = a.k > 0 ? nt * a.scale_cols : 0;
     uint32_t sc = 0;
-    if (tid >= 32 && tid - 32 < nsc) sc = a.x_scale[(int64_t)t_begin * a.scale_cols + tid - 32];
+    if (tid >= 32 && tid < 96 && tid - 32 < nsc)
+        sc = a.x_scale[(int64_t)t_begin * a.scale_cols + tid - 32];
 
     // the batch's picks; ids outside [-1, E) are reported (by block 0) and skipped
     for (int p = tid; p < P_all; p += kThreads) {
@@ -213,10 +214,10 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     __syncthreads();
 
     // warp 0 (thread 0) moves the rows: once they have landed, k bulk stores each
-    // from shared memory. Warps 1.. meanwhile copy the scale words (the ones loaded
-    // at the start), write this block's slice of m_indices and its tokens'
-    // is_token_in_rank rows, and tally the batch's tokens for this block's share of
-    // the rank and node columns.
+    // from shared memory. Meanwhile warps 1 and 2 copy the scale words (the ones
+    // loaded at the start), warp 3 writes this block's slice of m_indices, warp 4
+    // its tokens' is_token_in_rank rows, and warps 5.. tally the batch's tokens for
+    // this block's share of the rank and node columns.
     const int cols = a.R + (a.per_node ? a.N : 0);
     bool issued = false;  // this lane of warp 0 has bulk stores in flight
     if (warp == 0) {
@@ -241,9 +242,9 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
                 if (issued) bulk_commit();
             }
         }
-    } else {
-        const int wt = tid - 32, nwt = kThreads - 32;  // threads of warps 1..
-        for (int i = wt; i < nsc; i += nwt) {  // the first word of each thread is in sc
+    } else if (warp <= 2) {
+        const int wt = tid - 32;
+        for (int i = wt; i < nsc; i += 64) {  // the first word of each thread is in sc
             const int tl = i / a.scale_cols, c = i - tl * a.scale_cols;
             const uint32_t v = i == wt ? sc : a.x_scale[(int64_t)t_begin * a.scale_cols + i];
             for (int j = 0; j < a.k; ++j) {
@@ -251,12 +252,13 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
                 if (s >= 0) a.out_scale[(int64_t)s * a.scale_cols + c] = v;
             }
         }
-        // m_indices over this block's slice of the buffer: row s belongs to the last
-        // expert whose region starts at or before s, and holds it when it is among the
-        // region's first count rows (else -1: padding or rows past the last region)
+    } else if (warp == 3) {
+        // row s belongs to the last expert whose region starts at or before s, and
+        // holds it when it is among the region's first count rows (else -1: padding
+        // or rows past the last region)
         const int64_t m0 = a.capacity * blockIdx.x / gridDim.x;
         const int64_t m1 = a.capacity * (blockIdx.x + 1) / gridDim.x;
-        for (int64_t s = m0 + wt; s < m1; s += nwt) {
+        for (int64_t s = m0 + lane; s < m1; s += 32) {
             int lo = 0, hi = a.E - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -266,21 +268,24 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
             const int64_t st = s_start[lo];
             a.m_indices[s] = (s >= st && s < st + s_cnt[lo]) ? lo : -1;
         }
+    } else if (warp == 4) {
         if (a.in_rank)
-            for (int i = wt; i < nt * a.R; i += nwt) {
+            for (int i = lane; i < nt * a.R; i += 32) {
                 const int tl = i / a.R, r = i - tl * a.R;
                 const int16_t *row = s_e + (t_begin + tl) * a.k;
                 bool hit = false;
                 for (int j = 0; j < a.k && !hit; ++j) hit = row[j] >= 0 && s_rank_of[row[j]] == r;
                 a.in_rank[(int64_t)(t_begin + tl) * a.R + r] = hit ? 1 : 0;
             }
+    } else {
         // column cb of this block is col = blockIdx.x + cb * grid; 32 tokens per ballot
+        const int nwt = kThreads - 160;  // threads of warps 5..
         for (int cb = 0; cb < kSmallCols; ++cb) {
             const int col = blockIdx.x + cb * gridDim.x;
             if (col >= cols) break;
             const bool is_rank = col < a.R;
             const int target = is_rank ? col : col - a.R;
-            for (int t0 = (warp - 1) * 32; t0 < a.T; t0 += nwt) {
+            for (int t0 = (warp - 5) * 32; t0 < a.T; t0 += nwt) {
                 const int t = t0 + lane;
                 bool hit = false;
                 if (t < a.T) {
