@@ -10,6 +10,8 @@
  *                          buffer, with m_indices and output_index;
  *   4. ep_unpermute        combine: the topk-weighted sum of each token's expert
  *                          output rows, accumulated in fp32.
+ * ep_dispatch_layout_offsets runs steps 1 and 2 in one launch, and ep_dispatch
+ * steps 1 to 3 in one call (a single kernel for a decode-sized batch).
  * Nothing in between goes back to the host: every count, offset and total stays
  * in device memory, and the permuted buffer is sized at the T*k upper bound.
  *
