@@ -429,12 +429,17 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
     // bulk-copy kernel when at least two row stages fit in shared memory
     const TmaSmem L = tma_smem(a.row_bytes, k, a.e_end - a.e_begin);
     if (L.stages >= 2) {
-        static size_t opted = 0;
+        // the kernel's shared-memory limit, raised per device (a function attribute
+        // applies to the current device only)
+        static size_t opted_by_dev[64] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return record_cuda_error();
+        size_t scratch = 0;
+        size_t &opted = (dev >= 0 && dev < 64) ? opted_by_dev[dev] : scratch;
         if (L.total > opted) {
-            int dev = 0, optin = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-                    cudaSuccess)
+            int optin = 0;
+            if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
                 return record_cuda_error();
             if (L.total + 64 <= (size_t)optin) {
                 if (cudaFuncSetAttribute(permute_tma_kernel,
