@@ -28,7 +28,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 64, "header is one 64-byte block");
 
 constexpr size_t kAlign = 256;
-constexpr int kLayoutTilePairs = 2048;     // (token, pick) pairs per layout tile
+constexpr int kLayoutTilePairs = 1024;     // (token, pick) pairs per layout tile
 constexpr int kLayoutMaxTileTokens = 2048;
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -39,7 +39,7 @@ __host__ __device__ inline int layout_warps(int E) {
     return E <= 512 ? 32 : E <= 1024 ? 16 : E <= 2048 ? 8 : 4;
 }
 
-// Tokens per layout tile: at most 2048 pairs and at most 2048 tokens (one 64-bit
+// Tokens per layout tile: at most kLayoutTilePairs pairs and at most 2048 tokens (one 64-bit
 // rank mask and one node mask per token stay in shared memory).
 __host__ __device__ inline int layout_tile_tokens(int k) {
     const int t = k > 0 ? kLayoutTilePairs / k : kLayoutMaxTileTokens;
