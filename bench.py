@@ -588,18 +588,31 @@ def run_decode(args, rank, world, local):
         o["qs"] = torch.empty(E, H // 128, rows, dtype=torch.float32, device=dev)
         o["recv"] = torch.empty(E, dtype=torch.int32, device=dev)
         o["src"] = torch.empty(E, rows, dtype=torch.int32, device=dev)
+    # The fixed rectangles are one buffer, allocated once and reused by every step, as
+    # a serving loop does (470 MB of bf16 at decode_fp8: larger than L2 by itself).
+    # The exact layout's expert outputs are per input set (15 MB each; the pool keeps
+    # the inputs larger than L2).
+    rect = (torch.randn(E * rows, H, generator=gen, device=dev).to(torch.bfloat16)
+            if ll else None)
     inputs = [dict(topk=c.topk_idx.to(dev), w=c.topk_weights.to(dev), x=c.x.to(dev),
                    xs=None if c.x_scale is None else c.x_scale.to(dev),
-                   eo=(torch.randn(E * rows, H, generator=gen, device=dev).to(torch.bfloat16)
-                       if ll else c.expert_out.to(dev))) for c in pool]
+                   eo=rect if ll else c.expert_out.to(dev)) for c in pool]
 
     def chain_ll(inp, ev=None):
-        epd.ep_dispatch_layout(inp["topk"], E, R, N, ws, status, tokens_per_expert=o["per_e"],
-                               tokens_per_rank=o["per_r"], tokens_per_rdma_rank=o["per_n"],
-                               is_token_in_rank=o["itr"], stream=stream)
-        epd.ep_permute_lowlatency(inp["x"], inp["topk"], E, rows, ws, status, out_q=o["q"],
-                                  out_scale=o["qs"], recv_count=o["recv"],
-                                  output_index=o["out_idx"], src_token=o["src"], stream=stream)
+        if args.separate_offsets:  # the layout as its own launch, then the rectangle permute
+            epd.ep_dispatch_layout(inp["topk"], E, R, N, ws, status,
+                                   tokens_per_expert=o["per_e"], tokens_per_rank=o["per_r"],
+                                   tokens_per_rdma_rank=o["per_n"], is_token_in_rank=o["itr"],
+                                   stream=stream)
+            epd.ep_permute_lowlatency(inp["x"], inp["topk"], E, rows, ws, status, out_q=o["q"],
+                                      out_scale=o["qs"], recv_count=o["recv"],
+                                      output_index=o["out_idx"], src_token=o["src"],
+                                      stream=stream)
+        else:  # one call: one kernel for a decode batch
+            epd.ep_dispatch_lowlatency(inp["x"], inp["topk"], E, R, N, rows, ws, status,
+                                       out_q=o["q"], out_scale=o["qs"], recv_count=o["recv"],
+                                       output_index=o["out_idx"], src_token=o["src"],
+                                       stream=stream)
         if ev is not None:
             ev[0].record(stream)
         epd.ep_unpermute(inp["eo"], o["out_idx"], inp["w"], status, y=o["y"], stream=stream)
@@ -718,7 +731,9 @@ def run_decode(args, rank, world, local):
         "config": {"workload": "decode_fp8" + ("_lowlatency" if ll else ""), "tokens": T,
                    "hidden": H, "top_k": k, "experts": E,
                    "path": ("layout -> fixed-rectangle permute with bf16->e4m3 cast -> combine"
-                            if ll else
+                            if ll and args.separate_offsets else
+                            "ep_dispatch_lowlatency (fixed rectangles, bf16->e4m3 cast: one "
+                            "kernel) -> combine" if ll else
                             "ep_dispatch (layout, offsets, permute: one kernel) -> combine"
                             if args.dispatch else "layout -> offsets -> permute -> combine"),
                    "rows_per_expert": rows if ll else None,
@@ -739,8 +754,9 @@ def run_decode(args, rank, world, local):
                      "frac": round(bytes_k[dom] / (dom_us * 1e-6) / 1e9 / peak, 4),
                      "traffic": None, "algorithmic_bytes": bytes_k[dom],
                      "note": "latency-bound at this size; timed outside the graphs"},
-        "gpu_launches": (2 if args.dispatch and not ll else
-                         3 if ll or not args.separate_offsets else 4) * steps,
+        "gpu_launches": ((3 if args.separate_offsets else 2) if ll else
+                         2 if args.dispatch else
+                         3 if not args.separate_offsets else 4) * steps,
         "clocks": clocks.summary(),
         "e2e": None,
     }
@@ -822,7 +838,8 @@ def main(argv=None):
     ap.add_argument("--view-rank", type=int, default=None,
                     help="permute only this simulated rank's experts (local rows and ids)")
     ap.add_argument("--separate-offsets", action="store_true",
-                    help="run ep_dispatch_layout and ep_scan_offsets as two launches")
+                    help="run ep_dispatch_layout and ep_scan_offsets as two launches (with "
+                         "--lowlatency: the layout, then ep_permute_lowlatency)")
     ap.add_argument("--dispatch", action="store_true",
                     help="decode: ep_dispatch (layout, offsets and permute in one call: one "
                          "kernel for a decode batch) then ep_unpermute")

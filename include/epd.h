@@ -322,6 +322,27 @@ EPD_API epd_status_t ep_permute_lowlatency(const void *x_bf16, const int64_t *to
                                            int32_t *status, epd_stream_t stream);
 
 /*
+ * The low-latency dispatch in one call: the same outputs as ep_dispatch_layout (its
+ * pair ranks only) followed by ep_permute_lowlatency, without the layout's count
+ * outputs ([P3] low_latency_dispatch returns recv_count, not a layout). A
+ * decode-sized batch (T*k <= 4096, T <= 1024, E <= 1024, a block's bf16 rows
+ * within 96 KiB) runs as one kernel in which every block ranks its own tokens'
+ * picks against the batch itself -- a fixed rectangle needs no offsets -- and
+ * casts its own rows; the workspace is then not touched. Larger batches run the
+ * layout kernel (which needs `workspace` sized by epd_workspace_bytes(T, k, E, R,
+ * N)) and then ep_permute_lowlatency. Arguments, layouts, results and errors as in
+ * ep_permute_lowlatency.
+ */
+EPD_API epd_status_t ep_dispatch_lowlatency(const void *x_bf16, const int64_t *topk_idx,
+                                            int num_tokens, int num_topk, int hidden,
+                                            int num_experts, int num_ranks, int num_rdma_ranks,
+                                            int expert_begin, int expert_end,
+                                            int64_t rows_per_expert, void *workspace, void *out_q,
+                                            float *out_scale, int32_t *recv_count,
+                                            int32_t *output_index, int32_t *src_token,
+                                            int32_t *status, epd_stream_t stream);
+
+/*
  * Step 4 -- unpermute (combine). [P3] "Dispatch" (combine is the reverse of
  * dispatch; topk_weights are fp32 [T, k]):
  *   y[t, h] = bf16( sum over j with output_index[t, j] != -1, in j order, of

@@ -192,3 +192,24 @@ def test_dispatch_rejects_bad_args(lib):
     assert call(start=NULL) == E
     assert call(total=NULL) == E
     assert call(mi=NULL) == E
+
+
+def test_dispatch_lowlatency_rejects_bad_args(lib):
+    E = _binding.EPD_ERR_INVALID_ARG
+    f = lib.ep_dispatch_lowlatency
+    ok = dict(x=FAKE, topk=FAKE, T=4, k=2, H=128, E=8, R=4, N=2, b=0, e=8, rows=4, ws=FAKE,
+              q=FAKE, qs=FAKE, rc=FAKE, oi=FAKE, src=NULL, st=FAKE, s=NULL)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(*a.values())
+    assert call(H=64) == E                       # H % 128
+    assert call(R=3) == E                        # E % R
+    assert call(b=4, e=4) == E                   # empty view
+    assert call(e=9) == E                        # view past E
+    assert call(rows=-1) == E
+    assert call(ws=NULL) == E
+    assert call(rc=NULL) == E
+    assert call(st=NULL) == E
+    assert call(x=FAKE_ODD) == E                 # rows must be 16-byte aligned
+    assert call(q=NULL) == E                     # rectangles with rows but no buffer

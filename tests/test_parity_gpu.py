@@ -786,3 +786,96 @@ def test_dispatch_reports_invalid_ids_and_capacity():
     # aligned offsets with a buffer of only T*k rows: slots past it are reported
     g2 = _dispatch_path(case, alignment=64, capacity=100 * 4)
     assert g2.results()["status"] == epd.EPD_ERR_CAPACITY
+
+
+# ----------------------------------------------------------------------------- ep_dispatch_lowlatency
+def _ll_dispatch_compare(case, rows, b=0, e_end=None):
+    """ep_dispatch_lowlatency against the oracle (status from the oracle's overflow)."""
+    import oracle
+    dev = torch.device("cuda")
+    E = case.E
+    e_end = E if e_end is None else e_end
+    topk = case.topk_idx.to(dev)
+    x = case.x.to(dev)
+    ws = epd.new_workspace(case.T, case.k, E, case.R, case.N, dev)
+    st = epd.new_status(dev)
+    q, sc, rc, oi, src = epd.ep_dispatch_lowlatency(x, topk, E, case.R, case.N, rows, ws, st,
+                                                    expert_begin=b, expert_end=e_end)
+    torch.cuda.synchronize()
+    want = oracle.permute_lowlatency(bits16(case.x), case.topk_idx.numpy(), E, rows, b, e_end)
+    assert int(st.item()) == (epd.EPD_ERR_CAPACITY if want["overflow"] else 0)
+    got_oi = oi.cpu().numpy()
+    assert np.array_equal(got_oi, want["output_index"])
+    rcount = rc.cpu().numpy()
+    assert np.array_equal(rcount, want["recv_count"])
+    qb = q.cpu().view(torch.uint8).numpy().reshape(-1, case.H)
+    used = got_oi[got_oi >= 0]
+    assert np.array_equal(qb[used], want["out_q"].reshape(-1, case.H)[used])
+    gs = sc.cpu().numpy()
+    for e in range(e_end - b):
+        n = rcount[e]
+        assert np.array_equal(gs[e, :, :n], want["out_scale"][e, :, :n])
+        assert np.array_equal(src.cpu().numpy()[e, :n], want["src_token"][e, :n])
+    return oi
+
+
+LL_DISPATCH_CASES = [
+    # (name, T, H, k, E, R, N, routing, p_invalid, rows, view)
+    ("decode", 128, 7168, 8, 256, 32, 4, "uniform", 0.0, 128, None),
+    ("decode_rank_view", 128, 7168, 8, 256, 32, 4, "uniform", 0.0, 128, (40, 48)),
+    ("decode_overflow", 128, 1024, 8, 256, 32, 4, "repeats", 0.1, 3, None),
+    ("small_e", 300, 384, 4, 16, 8, 2, "repeats", 0.2, 300, (4, 12)),
+    ("k1_many_tokens", 1024, 256, 1, 64, 8, 1, "repeats", 0.1, 64, None),
+    ("k0", 50, 128, 0, 16, 8, 2, "uniform", 0.0, 4, None),
+    ("T0", 0, 128, 8, 16, 8, 2, "uniform", 0.0, 4, None),
+    ("two_kernels_prefill", 2048, 1024, 8, 256, 32, 4, "uniform", 0.0, 256, None),
+    ("two_kernels_many_experts", 200, 256, 8, 2048, 256, 8, "uniform", 0.0, 8, (0, 1024)),
+]
+
+
+@pytest.mark.parametrize("cfg", LL_DISPATCH_CASES, ids=[c[0] for c in LL_DISPATCH_CASES])
+def test_dispatch_lowlatency_matches_oracle(cfg):
+    _, T, H, k, E, R, N, routing, p_invalid, rows, view = cfg
+    case = workloads.make_random_case(T=T, H=H, k=k, E=E, R=R, N=N, dtype="bf16",
+                                      seed=T * 7 + k + E + rows, routing=routing,
+                                      p_invalid=p_invalid, experts="random")
+    b, e = view if view else (0, E)
+    _ll_dispatch_compare(case, rows, b, e)
+
+
+def test_dispatch_lowlatency_equals_two_calls():
+    """Same rows, scales, counts and sources as ep_dispatch_layout + ep_permute_lowlatency."""
+    case = _bf16_decode_case(T=128, seed=3100)
+    dev = torch.device("cuda")
+    topk, x = case.topk_idx.to(dev), case.x.to(dev)
+    ws1 = epd.new_workspace(case.T, case.k, case.E, case.R, case.N, dev)
+    ws2 = epd.new_workspace(case.T, case.k, case.E, case.R, case.N, dev)
+    st = epd.new_status(dev)
+    a = epd.ep_dispatch_lowlatency(x, topk, case.E, case.R, case.N, 128, ws1, st)
+    epd.ep_dispatch_layout(topk, case.E, case.R, case.N, ws2, st)
+    b = epd.ep_permute_lowlatency(x, topk, case.E, 128, ws2, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    oi = a[3].cpu().numpy()
+    used = oi[oi >= 0]
+    qa = a[0].view(torch.uint8).reshape(-1, case.H)
+    qb = b[0].view(torch.uint8).reshape(-1, case.H)
+    assert torch.equal(qa[used], qb[used])
+    for e in range(case.E):
+        n = int(a[2][e])
+        assert torch.equal(a[1][e, :, :n], b[1][e, :, :n])
+        assert torch.equal(a[4][e, :n], b[4][e, :n])
+
+
+def test_dispatch_lowlatency_reports_invalid_ids():
+    case = _bf16_decode_case(T=64, seed=3101)
+    bad = case.topk_idx.clone()
+    bad[5, 3] = 256
+    bad[60, 0] = -7
+    dev = torch.device("cuda")
+    ws = epd.new_workspace(case.T, case.k, case.E, case.R, case.N, dev)
+    st = epd.new_status(dev)
+    epd.ep_dispatch_lowlatency(case.x.to(dev), bad.to(dev), case.E, case.R, case.N, 64, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == epd.EPD_ERR_INVALID_EXPERT

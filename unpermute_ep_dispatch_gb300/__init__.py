@@ -21,7 +21,8 @@ from . import workloads  # noqa: F401  (CPU-only input generator)
 from ._binding import (  # noqa: F401,E402
     EPD_BF16, EPD_ERR_CAPACITY, EPD_ERR_CUDA, EPD_ERR_INVALID_ARG, EPD_ERR_INVALID_EXPERT,
     EPD_ERR_TIMEOUT, EPD_ERR_UNSUPPORTED, EPD_FP8_E4M3, EPD_OK, EpdError, check_status,
-    aligned_capacity, ep_dispatch, ep_dispatch_layout, ep_dispatch_layout_offsets, ep_permute,
+    aligned_capacity, ep_dispatch, ep_dispatch_layout, ep_dispatch_layout_offsets,
+    ep_dispatch_lowlatency, ep_permute,
     ep_permute_ex, ep_permute_lowlatency, ep_scan_offsets, ep_scan_offsets_aligned,
     ep_unpermute, epd_workspace_bytes,
     epd_workspace_init, load_library, new_status, new_workspace, status_string, version,

@@ -60,6 +60,8 @@ SIGNATURES = {
     "ep_unpermute": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P, _P]),
     "ep_permute_lowlatency": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P,
                                    _P, _P]),
+    "ep_dispatch_lowlatency": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P,
+                                    _P, _P, _P, _P]),
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "epd_test_layout_stalled_tile": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
                                           _U32, _P]),
@@ -478,6 +480,45 @@ def ep_permute_lowlatency(x: torch.Tensor, topk_idx: torch.Tensor, num_experts: 
         _ptr(out_q), _ptr(out_scale), _ptr(recv_count), _ptr(output_index), _ptr(src_token),
         _ptr(status), _stream(stream, dev))
     _check(rc, "ep_permute_lowlatency")
+    return out_q, out_scale, recv_count, output_index, src_token
+
+
+
+def ep_dispatch_lowlatency(x: torch.Tensor, topk_idx: torch.Tensor, num_experts: int,
+                           num_ranks: int, num_rdma_ranks: int, rows_per_expert: int,
+                           workspace: torch.Tensor, status: torch.Tensor, expert_begin: int = 0,
+                           expert_end: Optional[int] = None, out_q=None, out_scale=None,
+                           recv_count=None, output_index=None, src_token=None,
+                           with_src_token: bool = True, stream=None):
+    """The low-latency dispatch in one call (layout pair ranks, then the fixed-
+    rectangle permute with the fused cast; one kernel for a decode batch; see
+    epd.h). Returns what ep_permute_lowlatency returns."""
+    _want(x, "x", torch.bfloat16)
+    dev = x.device
+    T, H = x.shape
+    _want(topk_idx, "topk_idx", torch.int64, device=dev)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, k] with the T of x")
+    k = topk_idx.shape[1]
+    E, R, N = int(num_experts), int(num_ranks), int(num_rdma_ranks)
+    e_end = E if expert_end is None else int(expert_end)
+    EV = e_end - int(expert_begin)
+    rows = int(rows_per_expert)
+    _want(workspace, "workspace", torch.uint8, device=dev)
+    _want(status, "status", torch.int32, (1,), dev)
+    if workspace.numel() < epd_workspace_bytes(T, k, E, R, N):
+        raise ValueError("workspace too small for this layout")
+    out_q = _out(out_q, "out_q", torch.float8_e4m3fn, (EV, rows, H), dev)
+    out_scale = _out(out_scale, "out_scale", torch.float32, (EV, H // 128, rows), dev)
+    recv_count = _out(recv_count, "recv_count", torch.int32, (EV,), dev)
+    output_index = _out(output_index, "output_index", torch.int32, (T, k), dev)
+    if with_src_token:
+        src_token = _out(src_token, "src_token", torch.int32, (EV, rows), dev)
+    rc = load_library().ep_dispatch_lowlatency(
+        _ptr(x), _ptr(topk_idx), T, k, H, E, R, N, int(expert_begin), e_end, rows,
+        _ptr(workspace), _ptr(out_q), _ptr(out_scale), _ptr(recv_count), _ptr(output_index),
+        _ptr(src_token), _ptr(status), _stream(stream, dev))
+    _check(rc, "ep_dispatch_lowlatency")
     return out_q, out_scale, recv_count, output_index, src_token
 
 

@@ -90,6 +90,10 @@ inline bool topology_ok(int T, int k, int E, int R, int N) {
 
 int sm_count();  // multiprocessors of the current device (cached per device)
 
+// The layout kernel for its workspace only (no count outputs); layout.cu.
+epd_status_t layout_ranks_only(const int64_t *topk_idx, int T, int k, int E, int R, int N,
+                               void *workspace, int32_t *status, cudaStream_t stream);
+
 // Reads and clears the CUDA runtime's last error, keeps its code for
 // epd_last_cuda_error() and maps it to EPD_OK / EPD_ERR_CUDA.
 epd_status_t record_cuda_error();

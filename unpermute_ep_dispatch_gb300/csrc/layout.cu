@@ -383,14 +383,16 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         int part = 0, run = 0;
         for (int e = e0; e < e1; ++e) {
             const int tot = col_excl[e] + col_agg[e];
-            a.per_expert[e] = tot;
+            if (a.per_expert) a.per_expert[e] = tot;
             a.ws_counts[e] = tot;
             part += tot;
             run += (tot + a.alignment - 1) / a.alignment * a.alignment;
         }
         for (int c = a.E + tid; c < a.cols; c += kThreads) {
             const int tot = col_excl[c] + col_agg[c];
-            if (c < a.E + a.R) a.per_rank[c - a.E] = tot;
+            if (c < a.E + a.R) {
+                if (a.per_rank) a.per_rank[c - a.E] = tot;
+            }
             else if (a.per_node) a.per_node[c - a.E - a.R] = tot;
         }
         int incl = run;
@@ -479,7 +481,8 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
                            uint32_t spin_limit, cudaStream_t stream) {
     if (!topology_ok(T, k, E, R, N)) return EPD_ERR_INVALID_ARG;
     if ((int64_t)T * k > 0 && (topk_idx == nullptr || !aligned8(topk_idx))) return EPD_ERR_INVALID_ARG;
-    if (per_expert == nullptr || per_rank == nullptr || status == nullptr || workspace == nullptr)
+    // the count outputs are optional only for the internal ranks-only launch
+    if (status == nullptr || workspace == nullptr || (per_expert == nullptr) != (per_rank == nullptr))
         return EPD_ERR_INVALID_ARG;
     if (!aligned4(per_expert) || !aligned4(per_rank) || !aligned4(status) ||
         (per_node && !aligned4(per_node)) || !aligned16(workspace))
@@ -594,6 +597,7 @@ epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens, int num
                                 int32_t *tokens_per_expert, int32_t *tokens_per_rank,
                                 int32_t *tokens_per_rdma_rank, uint8_t *is_token_in_rank,
                                 void *workspace, int32_t *status, epd_stream_t stream) {
+    if (!tokens_per_expert || !tokens_per_rank) return EPD_ERR_INVALID_ARG;
     return epd::layout_launch(nullptr, nullptr, 1, topk_idx, num_tokens, num_topk, num_experts, num_ranks,
                               num_rdma_ranks, tokens_per_expert, tokens_per_rank,
                               tokens_per_rdma_rank, is_token_in_rank, workspace, status, -1,
@@ -608,7 +612,8 @@ epd_status_t ep_dispatch_layout_offsets(const int64_t *topk_idx, int num_tokens,
                                         int32_t *total_rows, void *workspace, int32_t *status,
                                         epd_stream_t stream) {
     if (alignment < 1 || alignment > EPD_MAX_ALIGNMENT || !expert_start_loc || !total_rows ||
-        !epd::aligned4(expert_start_loc) || !epd::aligned4(total_rows))
+        !epd::aligned4(expert_start_loc) || !epd::aligned4(total_rows) || !tokens_per_expert ||
+        !tokens_per_rank)
         return EPD_ERR_INVALID_ARG;
     return epd::layout_launch(expert_start_loc, total_rows, alignment, topk_idx, num_tokens,
                               num_topk, num_experts, num_ranks, num_rdma_ranks, tokens_per_expert,
@@ -624,7 +629,9 @@ epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_token
                                           uint8_t *is_token_in_rank, void *workspace,
                                           int32_t *status, int stalled_tile,
                                           uint32_t spin_limit, epd_stream_t stream) {
-    if (stalled_tile < 0 || spin_limit > epd::kDefaultSpinLimit) return EPD_ERR_INVALID_ARG;
+    if (stalled_tile < 0 || spin_limit > epd::kDefaultSpinLimit || !tokens_per_expert ||
+        !tokens_per_rank)
+        return EPD_ERR_INVALID_ARG;
     return epd::layout_launch(nullptr, nullptr, 1, topk_idx, num_tokens, num_topk, num_experts, num_ranks,
                               num_rdma_ranks, tokens_per_expert, tokens_per_rank,
                               tokens_per_rdma_rank, is_token_in_rank, workspace, status,
@@ -632,6 +639,17 @@ epd_status_t epd_test_layout_stalled_tile(const int64_t *topk_idx, int num_token
 }
 
 }  // extern "C"
+
+namespace epd {
+// The layout kernel for its workspace only (pair ranks, counts, header): no
+// count outputs. Used by ep_dispatch_lowlatency for batches beyond its one-kernel
+// form.
+epd_status_t layout_ranks_only(const int64_t *topk_idx, int T, int k, int E, int R, int N,
+                               void *workspace, int32_t *status, cudaStream_t stream) {
+    return layout_launch(nullptr, nullptr, 1, topk_idx, T, k, E, R, N, nullptr, nullptr, nullptr,
+                         nullptr, workspace, status, -1, kDefaultSpinLimit, stream);
+}
+}  // namespace epd
 
 // ---------------------------------------------------------------------------- allocation-free variant
 // Scratch for ep_dispatch_layout_noalloc: a file-scope device array that every

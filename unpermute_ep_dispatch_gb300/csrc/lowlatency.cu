@@ -172,6 +172,181 @@ __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
     pdl_trigger();
 }
 
+// ----------------------------------------------------------------------------- one kernel
+// ep_dispatch_lowlatency for a decode-sized batch: no layout kernel. Blocks
+// (x, y) share the token run x: every one reads the batch's picks into shared
+// memory and ranks the run's pairs (the number of earlier pairs, in row-major
+// order, with the same expert), which is all a fixed rectangle needs; it
+// bulk-loads the run's bf16 rows into shared memory as it starts and casts the
+// units (token, two 128-column blocks) u = y, y + gridDim.y, ... from there. Blocks
+// with y = 0 write output_index and src_token; block (0, 0) counts the view's
+// experts for recv_count.
+constexpr int kLLSmallPairs = 4096;
+constexpr int kLLSmallExperts = 1024;
+constexpr int kLLSmallTokens = 1024;
+constexpr int kLLSmallBlockPairs = 128;
+constexpr size_t kLLSmallRowBytes = 96 * 1024;
+constexpr uint32_t kLLWaitLimit = 1u << 24;
+
+struct LLSmallArgs {
+    const uint8_t *x;  // bf16 [T, H]
+    int T, k, H, E, e_begin, e_end;
+    int64_t rows;
+    const int64_t *topk;
+    uint8_t *out_q;
+    float *out_scale;
+    int32_t *recv_count, *output_index, *src_token, *status;
+};
+
+__host__ __device__ inline size_t ll_row_stride(int H) { return align_up((size_t)H * 2, 128); }
+
+__global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs a) {
+    extern __shared__ __align__(128) uint8_t s_x[];  // the block's bf16 rows
+    __shared__ int16_t s_e[kLLSmallPairs];
+    __shared__ int s_cnt[kLLSmallExperts];            // block 0: picks per expert of the view
+    __shared__ int s_rank[kLLSmallBlockPairs], s_row[kLLSmallBlockPairs];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ int s_ok;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P_all = a.T * a.k;
+    const int EV = a.e_end - a.e_begin;
+    const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
+    const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    const int nt = t_end - t_begin;
+    const size_t stride = ll_row_stride(a.H);
+    const bool copy = a.k > 0 && nt > 0;
+    const bool lead = blockIdx.y == 0;                  // writes the run's indices
+    const bool first = lead && blockIdx.x == 0;         // writes recv_count
+    if (first)
+        for (int e = tid; e < EV; e += kThreads) s_cnt[e] = 0;
+    for (int q = tid; q < kLLSmallBlockPairs; q += kThreads) s_rank[q] = 0;
+    if (tid == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_init_fence();
+    }
+    pdl_wait();  // topk_idx and the rows may come from the previous kernel
+
+    if (tid == 0 && copy) {
+        const uint32_t bytes = (uint32_t)a.H * 2;
+        mbar_expect_tx(&s_bar, (uint32_t)nt * bytes);
+        for (int tl = 0; tl < nt; ++tl)
+            bulk_load(s_x + tl * stride, a.x + (int64_t)(t_begin + tl) * bytes, bytes, &s_bar);
+    }
+    for (int p = tid; p < P_all; p += kThreads) {
+        const int64_t v = a.topk[p];
+        const bool ok = v >= 0 && v < a.E;
+        if ((v < -1 || v >= a.E) && first) report(a.status, EPD_ERR_INVALID_EXPERT);
+        s_e[p] = ok ? (int16_t)v : (int16_t)-1;
+    }
+    __syncthreads();
+    if (first)
+        for (int p = tid; p < P_all; p += kThreads) {
+            const int e = s_e[p];
+            if (e >= a.e_begin && e < a.e_end) atomicAdd(&s_cnt[e - a.e_begin], 1);
+        }
+    // ranks of this block's pairs: every thread checks its share of the batch against
+    // up to 16 of the block's pairs at a time (sparse shared-memory atomics)
+    const int p0 = t_begin * a.k, q_end = nt * a.k;
+    for (int g0 = 0; g0 < q_end; g0 += 16) {
+        int ge[16], cnt[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int e = g0 + j < q_end ? s_e[p0 + g0 + j] : -2;
+            ge[j] = (e >= a.e_begin && e < a.e_end) ? e : -2;  // only the view's picks get rows
+            cnt[j] = 0;
+        }
+        const int pmax = p0 + min(q_end, g0 + 16);
+        for (int pp = tid; pp < pmax; pp += kThreads) {
+            const int e = s_e[pp];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cnt[j] += (e == ge[j]) & (pp < p0 + g0 + j);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (cnt[j]) atomicAdd(&s_rank[g0 + j], cnt[j]);
+    }
+    __syncthreads();
+    // rows in the rectangles; a pick past its rectangle is dropped and reported
+    for (int q = tid; q < q_end; q += kThreads) {
+        const int p = p0 + q;
+        const int e = s_e[p];
+        int row = -1;
+        if (e >= a.e_begin && e < a.e_end) {
+            const int64_t r = s_rank[q];
+            if (r < a.rows) {
+                row = (int)((e - a.e_begin) * a.rows + r);
+                if (lead && a.src_token) a.src_token[row] = t_begin + q / a.k;
+            } else if (lead) {
+                report(a.status, EPD_ERR_CAPACITY);
+            }
+        }
+        if (lead) a.output_index[p] = row;
+        s_row[q] = row;
+    }
+    if (first) {
+        __syncthreads();
+        for (int e = tid; e < EV; e += kThreads) {
+            const int64_t c = s_cnt[e];
+            a.recv_count[e] = (int32_t)(c < a.rows ? c : a.rows);
+        }
+    }
+    // the rows have landed (every thread observes the barrier before reading them)
+    if (tid == 0) s_ok = 1;
+    __syncthreads();
+    if (copy && !mbar_wait_bounded(&s_bar, 0u, kLLWaitLimit)) {
+        if (tid == 0) report(a.status, EPD_ERR_TIMEOUT);
+        s_ok = 0;
+    }
+    __syncthreads();
+    // cast: units of (token, two 128-column blocks), a half-warp per block
+    const int C = a.H >> 7, upt = (C + 1) >> 1;
+    const int half = lane >> 4, hl = lane & 15;
+    if (s_ok && copy)
+        for (int u = blockIdx.y * kWarps + warp; u < nt * upt; u += gridDim.y * kWarps) {
+            const int tl = u / upt, ch = u - tl * upt;
+            const int c = 2 * ch + half;
+            const int *rows = s_row + tl * a.k;
+            bool any = false;
+            for (int j = 0; j < a.k; ++j) any |= rows[j] >= 0;
+            if (!any) continue;  // warp-uniform: the token has no row in the view
+            const bool active = c < C;
+            float v[8];
+            float amax = 0.0f;
+            if (active) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(s_x + tl * stride + (128 * c + 8 * hl) * 2);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = __uint_as_float(w[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (!active) continue;
+            const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            uint2 qv;
+            qv.x = e4m3x4(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale), __fdiv_rn(v[2], scale),
+                          __fdiv_rn(v[3], scale));
+            qv.y = e4m3x4(__fdiv_rn(v[4], scale), __fdiv_rn(v[5], scale), __fdiv_rn(v[6], scale),
+                          __fdiv_rn(v[7], scale));
+            for (int j = 0; j < a.k; ++j) {
+                const int row = rows[j];
+                if (row < 0) continue;
+                *reinterpret_cast<uint2 *>(a.out_q + (int64_t)row * a.H + 128 * c + 8 * hl) = qv;
+                if (hl == 0) {
+                    const int64_t el = row / a.rows, r = row - el * a.rows;
+                    a.out_scale[(el * C + c) * a.rows + r] = scale;
+                }
+            }
+        }
+    // loads that outlived a wait that gave up land before shared memory is released
+    if (tid == 0 && copy && !s_ok) mbar_wait_bounded(&s_bar, 0u, kLLWaitLimit);
+    pdl_trigger();
+}
+
 }  // namespace
 }  // namespace epd
 
@@ -226,4 +401,91 @@ extern "C" epd_status_t ep_permute_lowlatency(const void *x_bf16, const int64_t 
     const int grid = (int)(want < 1 ? 1 : (want < full ? want : full));
     return launch_pdl(lowlatency_kernel, grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream),
                       a);
+}
+
+extern "C" epd_status_t ep_dispatch_lowlatency(const void *x_bf16, const int64_t *topk_idx,
+                                               int num_tokens, int num_topk, int hidden,
+                                               int num_experts, int num_ranks, int num_rdma_ranks,
+                                               int expert_begin, int expert_end,
+                                               int64_t rows_per_expert, void *workspace,
+                                               void *out_q, float *out_scale,
+                                               int32_t *recv_count, int32_t *output_index,
+                                               int32_t *src_token, int32_t *status,
+                                               epd_stream_t stream) {
+    using namespace epd;
+    const int T = num_tokens, k = num_topk, H = hidden, E = num_experts;
+    if (!topology_ok(T, k, E, num_ranks, num_rdma_ranks)) return EPD_ERR_INVALID_ARG;
+    if (H < 128 || H % 128 != 0) return EPD_ERR_INVALID_ARG;
+    if (expert_begin < 0 || expert_end > E || expert_begin >= expert_end) return EPD_ERR_INVALID_ARG;
+    const int64_t EV = expert_end - expert_begin;
+    if (rows_per_expert < 0 || EV * rows_per_expert > INT32_MAX) return EPD_ERR_INVALID_ARG;
+    if (!workspace || !recv_count || !status || !aligned16(workspace) || !aligned4(recv_count) ||
+        !aligned4(status))
+        return EPD_ERR_INVALID_ARG;
+    if ((int64_t)T * k > 0 && (!x_bf16 || !topk_idx || !output_index)) return EPD_ERR_INVALID_ARG;
+    if (EV * rows_per_expert > 0 && (!out_q || !out_scale)) return EPD_ERR_INVALID_ARG;
+    if ((x_bf16 && !aligned16(x_bf16)) || (topk_idx && !aligned8(topk_idx)) ||
+        (out_q && !aligned8(out_q)) || !aligned4(out_scale) || !aligned4(output_index) ||
+        !aligned4(src_token))
+        return EPD_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid_cap = 2 * sm_count();
+    const int grid = T < 1 ? 1 : (T < grid_cap ? T : grid_cap);
+    const int tokens_per_block = T > 0 ? (T + grid - 1) / grid : 0;
+    const size_t smem = (size_t)tokens_per_block * ll_row_stride(H);
+    const bool small = (int64_t)T * k <= kLLSmallPairs && T <= kLLSmallTokens &&
+                       E <= kLLSmallExperts && (int64_t)tokens_per_block * k <= kLLSmallBlockPairs &&
+                       smem <= kLLSmallRowBytes;
+    if (!small) {
+        const epd_status_t st = layout_ranks_only(topk_idx, T, k, E, num_ranks, num_rdma_ranks,
+                                                  workspace, status, s);
+        if (st != EPD_OK) return st;
+        return ep_permute_lowlatency(x_bf16, topk_idx, T, k, H, E, expert_begin, expert_end,
+                                     rows_per_expert, workspace, out_q, out_scale, recv_count,
+                                     output_index, src_token, status, stream);
+    }
+    static bool opted[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return record_cuda_error();
+    if (dev < 0 || dev >= 64 || !opted[dev]) {
+        if (cudaFuncSetAttribute(lowlatency_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kLLSmallRowBytes) != cudaSuccess)
+            return record_cuda_error();
+        if (dev >= 0 && dev < 64) opted[dev] = true;
+    }
+    LLSmallArgs a;
+    a.x = static_cast<const uint8_t *>(x_bf16);
+    a.T = T;
+    a.k = k;
+    a.H = H;
+    a.E = E;
+    a.e_begin = expert_begin;
+    a.e_end = expert_end;
+    a.rows = rows_per_expert;
+    a.topk = topk_idx;
+    a.out_q = static_cast<uint8_t *>(out_q);
+    a.out_scale = out_scale;
+    a.recv_count = recv_count;
+    a.output_index = output_index;
+    a.src_token = src_token;
+    a.status = status;
+    // blocks per token run: enough to give every warp one unit of the cast, within
+    // four blocks per SM in all
+    const int upt = (H / 128 + 1) / 2;
+    const int units_per_run = tokens_per_block * upt;
+    int split = (units_per_run + kWarps - 1) / kWarps;
+    const int split_cap = (4 * sm_count()) / grid;
+    split = split < 1 ? 1 : (split > split_cap ? (split_cap < 1 ? 1 : split_cap) : split);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, (unsigned)split);
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, lowlatency_small_kernel, a);
+    return record_cuda_error();
 }
