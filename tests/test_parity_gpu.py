@@ -570,8 +570,9 @@ _TOPOS = [(1, 1, 1), (2, 2, 1), (4, 2, 2), (16, 8, 2), (64, 8, 1), (96, 12, 3), 
 def _sweep_config(i):
     """Configuration i of the sweep, drawn from its own seed: topology, k (0 and 64
     included), T across tile boundaries, dtype and row width, routing style, dropped
-    picks, alignment and whether the offsets are fused into the layout launch. Rows
-    are kept to a few MB so that the oracle finishes in well under a second."""
+    picks, alignment, whether the offsets are fused into the layout launch, and
+    whether ep_dispatch runs the first three steps. Rows are kept to a few MB so
+    that the oracle finishes in well under a second."""
     rng = np.random.default_rng(9000 + i)
     E, R, N = _TOPOS[int(rng.integers(len(_TOPOS)))]
     k = int(rng.choice([0, 1, 2, 3, 4, 6, 8, 9, 16, 64]))
@@ -591,8 +592,9 @@ def _sweep_config(i):
     p_invalid = float(rng.choice([0.0, 0.1, 0.5]))
     alignment = int(rng.choice([1, 1, 4, 64, 128]))
     fused = bool(rng.integers(2))
+    dispatch = bool(rng.integers(3) == 0)  # layout, offsets and permute through ep_dispatch
     return dict(E=E, R=R, N=N, k=k, T=T, dtype=dtype, H=H, routing=routing,
-                p_invalid=p_invalid, alignment=alignment, fused=fused)
+                p_invalid=p_invalid, alignment=alignment, fused=fused, dispatch=dispatch)
 
 
 @pytest.mark.parametrize("i", range(40))
@@ -602,8 +604,11 @@ def test_random_sweep(i):
                                       R=cfg["R"], N=cfg["N"], dtype=cfg["dtype"], seed=9100 + i,
                                       routing=cfg["routing"], p_invalid=cfg["p_invalid"],
                                       experts="random", zero_experts=20)
-    g = GpuPath(case, alignment=cfg["alignment"], fused=cfg["fused"])
-    g.step()
+    if cfg["dispatch"]:
+        g = _dispatch_path(case, alignment=cfg["alignment"])
+    else:
+        g = GpuPath(case, alignment=cfg["alignment"], fused=cfg["fused"])
+        g.step()
     got = g.results()
     want = oracle_path(case, alignment=cfg["alignment"])
     compare(got, want)
