@@ -529,7 +529,8 @@ def run_epd(args, rank, world, local):
                         f"step); the others from a separate "
                         f"{n_prof}-step pass with events around every kernel",
         # column-major scales add the scale pass after the row copy (inside ep_permute_ex)
-        "gpu_launches": ((3 if fused else 4) + (1 if scale_pass else 0)) * args.steps,
+        # every rank's kernels in the timed region (the job's total, like value)
+        "gpu_launches": ((3 if fused else 4) + (1 if scale_pass else 0)) * args.steps * world,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
@@ -756,7 +757,7 @@ def run_decode(args, rank, world, local):
                      "note": "latency-bound at this size; timed outside the graphs"},
         "gpu_launches": ((3 if args.separate_offsets else 2) if ll else
                          2 if args.dispatch else
-                         3 if not args.separate_offsets else 4) * steps,
+                         3 if not args.separate_offsets else 4) * steps * world,
         "clocks": clocks.summary(),
         "e2e": None,
     }
