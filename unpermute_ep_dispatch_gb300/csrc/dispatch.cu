@@ -33,7 +33,6 @@ namespace epd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kSmallPairs = 4096;     // T*k of the one-kernel form
 constexpr int kSmallExperts = 1024;   // E of the one-kernel form
 constexpr int kSmallTokens = 1024;    // T of the one-kernel form (block 0 counts every token)
@@ -87,7 +86,6 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     __shared__ int s_start[kSmallExperts];  // (aligned) offsets
     __shared__ uint8_t s_rank_of[kSmallExperts], s_node_of[64];
     __shared__ int s_rank[kSmallBlockPairs], s_slot[kSmallBlockPairs];
-    __shared__ int s_wsum[kWarps], s_wpairs[kWarps];
     __shared__ int s_total, s_pairs;
     __shared__ bool s_rows_ok;
     __shared__ int s_col[kSmallCols];  // this block's tallies of tokens per rank / node
@@ -125,46 +123,26 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     if (tid >= 32 && tid < 96 && tid - 32 < nsc)
         sc = a.x_scale[(int64_t)t_begin * a.scale_cols + tid - 32];
 
-    // the batch's picks; ids outside [-1, E) are reported (by block 0) and skipped
+    // the batch's picks, counted per expert as they arrive; ids outside [-1, E) are
+    // reported (by block 0) and skipped
     for (int p = tid; p < P_all; p += kThreads) {
         const int64_t v = a.topk[p];
         const bool ok = v >= 0 && v < a.E;
         if ((v < -1 || v >= a.E) && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_EXPERT);
         s_e[p] = ok ? (int16_t)v : (int16_t)-1;
-    }
-    __syncthreads();
-    for (int p = tid; p < P_all; p += kThreads) {
-        const int e = s_e[p];
-        if (e >= 0) atomicAdd(&s_cnt[e], 1);
-    }
-    // ranks of this block's pairs (the number of earlier pairs with the same expert):
-    // every thread checks its share of the batch against up to 16 of the block's
-    // pairs at a time, then a block reduction
-    const int p0 = t_begin * a.k, q_end = nt * a.k;
-    for (int g0 = 0; g0 < q_end; g0 += 16) {
-        int ge[16], cnt[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            ge[j] = g0 + j < q_end ? s_e[p0 + g0 + j] : -2;
-            cnt[j] = 0;
-        }
-        const int pmax = p0 + min(q_end, g0 + 16);
-        for (int pp = tid; pp < pmax; pp += kThreads) {
-            const int e = s_e[pp];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) cnt[j] += (e == ge[j]) & (pp < p0 + g0 + j);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)  // nearly every count is 0: sparse atomics
-            if (cnt[j]) atomicAdd(&s_rank[g0 + j], cnt[j]);
+        if (ok) atomicAdd(&s_cnt[(int)v], 1);
     }
     __syncthreads();
 
-    // exclusive prefix sum of the (aligned) counts: each thread a contiguous run of
-    // experts, a warp-shuffle scan of the runs, then of the warps' sums
-    {
-        const int per = (a.E + kThreads - 1) / kThreads;
-        const int e0 = min(a.E, tid * per), e1 = min(a.E, e0 + per);
+    // warp 0: exclusive prefix sum of the (aligned) counts, each lane a contiguous run
+    // of up to 32 experts, then a shuffle scan of the runs. Meanwhile warps 1..: ranks
+    // of this block's pairs (the number of earlier pairs with the same expert), every
+    // thread checking its share of the batch against up to 16 of the block's pairs at
+    // a time (sparse shared-memory atomics).
+    const int p0 = t_begin * a.k, q_end = nt * a.k;
+    if (warp == 0) {
+        const int per = (a.E + 31) / 32;
+        const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
         int run = 0, pairs = 0;
         for (int e = e0; e < e1; ++e) {
             const int c = s_cnt[e];
@@ -173,27 +151,31 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
         }
         const int incl = warp_incl_scan(run, lane);
         pairs = warp_sum(pairs);
-        if (lane == 31) {
-            s_wsum[warp] = incl;
-            s_wpairs[warp] = pairs;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const int v = lane < kWarps ? s_wsum[lane] : 0;
-            const int wincl = warp_incl_scan(v, lane);
-            const int P = warp_sum(lane < kWarps ? s_wpairs[lane] : 0);
-            if (lane < kWarps) s_wsum[lane] = wincl - v;
-            if (lane == 31) {
-                s_total = wincl;
-                s_pairs = P;
-            }
-        }
-        __syncthreads();
-        int pos = s_wsum[warp] + incl - run;
+        int pos = incl - run;
         for (int e = e0; e < e1; ++e) {
             s_start[e] = pos;
             pos += (s_cnt[e] + a.alignment - 1) / a.alignment * a.alignment;
         }
+        if (lane == 31) {
+            s_total = incl;
+            s_pairs = pairs;
+        }
+    } else for (int g0 = 0; g0 < q_end; g0 += 16) {
+        int ge[16], cnt[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            ge[j] = g0 + j < q_end ? s_e[p0 + g0 + j] : -2;
+            cnt[j] = 0;
+        }
+        const int pmax = p0 + min(q_end, g0 + 16);
+        for (int pp = tid - 32; pp < pmax; pp += kThreads - 32) {
+            const int e = s_e[pp];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cnt[j] += (e == ge[j]) & (pp < p0 + g0 + j);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)  // nearly every count is 0: sparse atomics
+            if (cnt[j]) atomicAdd(&s_rank[g0 + j], cnt[j]);
     }
     __syncthreads();
 
