@@ -686,9 +686,9 @@ def test_random_sweep_permute_ex(i):
 
 @pytest.mark.parametrize("i", range(12))
 def test_random_sweep_lowlatency(i):
-    """ep_permute_lowlatency over random sizes, views and rectangle heights (some
-    too small, which must report EPD_ERR_CAPACITY and drop exactly the oracle's
-    picks), against the oracle."""
+    """ep_permute_lowlatency (even i) and ep_dispatch_lowlatency (odd i) over random
+    sizes, views and rectangle heights (some too small, which must report
+    EPD_ERR_CAPACITY and drop exactly the oracle's picks), against the oracle."""
     import oracle
     rng = np.random.default_rng(9700 + i)
     E, R, N = _TOPOS[int(rng.integers(3, 8))]
@@ -700,6 +700,9 @@ def test_random_sweep_lowlatency(i):
                                       experts="random")
     b, e = _sweep_view(rng, E, R)
     rows = int(rng.choice([1, 4, max(1, T * k // max(E, 1)), T]))
+    if i % 2:  # the one-call form (one kernel for these sizes)
+        _ll_dispatch_compare(case, rows, b, e)
+        return
     want = oracle.permute_lowlatency(bits16(case.x), case.topk_idx.numpy(), E, rows, b, e)
     _ll_compare(case, rows=rows, b=b, e_end=e,
                 expect_status=epd.EPD_ERR_CAPACITY if want["overflow"] else 0)
