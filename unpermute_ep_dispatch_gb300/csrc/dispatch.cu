@@ -27,6 +27,8 @@
 // workspace as the layout kernel would (header, counts, pair ranks), so a later
 // ep_permute on the same workspace sees the same state. Larger batches run the
 // layout and permute kernels.
+#include <atomic>
+
 #include "epd_common.cuh"
 
 namespace epd {
@@ -408,14 +410,14 @@ extern "C" epd_status_t ep_dispatch(const void *x, epd_dtype_t dtype, const floa
     a.status = status;
     // the static arrays and up to kSmallRowBytes of rows exceed the default 48 KiB
     // limit: opt in once per device
-    static bool opted[64] = {false};
+    static std::atomic<bool> opted[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return record_cuda_error();
-    if (dev < 0 || dev >= 64 || !opted[dev]) {
+    if (dev < 0 || dev >= 64 || !opted[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(small_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmallRowBytes) != cudaSuccess)
             return record_cuda_error();
-        if (dev >= 0 && dev < 64) opted[dev] = true;
+        if (dev >= 0 && dev < 64) opted[dev].store(true, std::memory_order_release);
     }
     return launch_pdl(small_dispatch_kernel, grid, kThreads, smem, s, a);
 }

@@ -546,7 +546,7 @@ epd_status_t record_cuda_error() {
 }
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
     if (dev < 0 || dev >= 64) dev = 0;

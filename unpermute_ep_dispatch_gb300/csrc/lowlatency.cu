@@ -21,6 +21,8 @@
 // first store.
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "epd_common.cuh"
 
 namespace epd {
@@ -393,8 +395,7 @@ extern "C" epd_status_t ep_permute_lowlatency(const void *x_bf16, const int64_t 
     a.output_index = output_index;
     a.src_token = src_token;
     a.status = status;
-    static int resident = 0;
-    if (resident == 0) resident = blocks_per_sm(lowlatency_kernel, kThreads, 0);
+    static const int resident = blocks_per_sm(lowlatency_kernel, kThreads, 0);
     const int64_t units = (int64_t)T * ((H / 128 + 1) / 2);
     const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = (int64_t)sm_count() * resident;
@@ -444,14 +445,14 @@ extern "C" epd_status_t ep_dispatch_lowlatency(const void *x_bf16, const int64_t
                                      rows_per_expert, workspace, out_q, out_scale, recv_count,
                                      output_index, src_token, status, stream);
     }
-    static bool opted[64] = {false};
+    static std::atomic<bool> opted[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return record_cuda_error();
-    if (dev < 0 || dev >= 64 || !opted[dev]) {
+    if (dev < 0 || dev >= 64 || !opted[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(lowlatency_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kLLSmallRowBytes) != cudaSuccess)
             return record_cuda_error();
-        if (dev >= 0 && dev < 64) opted[dev] = true;
+        if (dev >= 0 && dev < 64) opted[dev].store(true, std::memory_order_release);
     }
     LLSmallArgs a;
     a.x = static_cast<const uint8_t *>(x_bf16);

@@ -14,6 +14,8 @@
 // no SM idles in a tail wave. Each unit is read once (16-byte streaming loads
 // that bypass L1) and written k times with 16-byte coalesced stores: every
 // warp-wide store covers 512 contiguous bytes of a destination row.
+#include <atomic>
+
 #include "epd_common.cuh"
 
 namespace epd {
@@ -431,12 +433,12 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
     if (L.stages >= 2) {
         // the kernel's shared-memory limit, raised per device (a function attribute
         // applies to the current device only)
-        static size_t opted_by_dev[64] = {0};
+        static std::atomic<size_t> opted_by_dev[64];
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return record_cuda_error();
-        size_t scratch = 0;
-        size_t &opted = (dev >= 0 && dev < 64) ? opted_by_dev[dev] : scratch;
-        if (L.total > opted) {
+        std::atomic<size_t> scratch{0};
+        std::atomic<size_t> &opted = (dev >= 0 && dev < 64) ? opted_by_dev[dev] : scratch;
+        if (L.total > opted.load(std::memory_order_acquire)) {
             int optin = 0;
             if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
                 cudaSuccess)
@@ -446,18 +448,17 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L.total) != cudaSuccess)
                     return record_cuda_error();
-                opted = L.total;
+                opted.store(L.total, std::memory_order_release);
             }
         }
-        if (L.total <= opted) {
+        if (L.total <= opted.load(std::memory_order_acquire)) {
             // three blocks' worth of token runs per SM (measured best on GB300)
             const int64_t full = 3 * (int64_t)sm_count();
             const int grid = (int)(T < full ? (T < 1 ? 1 : T) : full);
             return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
         }
     }
-    static int resident = 0;
-    if (resident == 0) resident = blocks_per_sm(permute_kernel, kThreads, 0);
+    static const int resident = blocks_per_sm(permute_kernel, kThreads, 0);
     const int64_t units = T * ((a.row_bytes / 16 + kUnitVecs - 1) / kUnitVecs);
     const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = (int64_t)sm_count() * resident;

@@ -134,8 +134,7 @@ __global__ void __launch_bounds__(kThreads) unpermute_kernel(UnpermuteArgs a) {
 
 template <int KT, int U>
 epd_status_t launch(const UnpermuteArgs &a, cudaStream_t stream) {
-    static int resident = 0;
-    if (resident == 0) resident = blocks_per_sm(unpermute_kernel<KT, U>, kThreads, 0);
+    static const int resident = blocks_per_sm(unpermute_kernel<KT, U>, kThreads, 0);
     const int64_t units = (int64_t)a.T * ((a.row_vecs + 32 * U - 1) / (32 * U));
     const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = (int64_t)sm_count() * resident;
