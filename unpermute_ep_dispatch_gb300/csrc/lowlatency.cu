@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
     pdl_wait();  // pair ranks and counts come from the layout kernel
     // Each warp checks the workspace header itself, and every load that does not
     // depend on a slot (the header, the row, the picks and their ranks) is issued
-    // before the first store, which waits for the header's verdict.
+    // before the first store, which waits for the header check's result.
     int hdr_ok = 0;
     if (lane == 0) hdr_ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
     bool checked = false;
