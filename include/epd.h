@@ -33,12 +33,11 @@
  *   - Kernels are launched with programmatic dependent launch: a kernel may
  *     start while the kernel before it on the stream drains, and waits
  *     (griddepcontrol.wait) before it reads what that kernel may write; every
- *     libepd kernel waits before it lets its own dependents start. The layout
- *     calls take the workspace's tile ticket before that wait, so the kernel
- *     launched immediately before them must not write the workspace, and a
- *     workspace's previous call must be complete by the time the kernel before
- *     the layout starts (always so when the kernels in between are libepd's or
- *     were launched without programmatic serialization).
+ *     libepd kernel waits before it lets its own dependents start. Calls on one
+ *     stream may follow each other in any order on one workspace -- two layout
+ *     calls back to back included: a layout kernel takes its tile ticket before
+ *     that wait from a counter that every call returns to zero, and reads the
+ *     rest of the workspace only after it.
  *   - Sizes: T = num_tokens >= 0, k = num_topk in [0, EPD_MAX_TOPK],
  *     E = num_experts in [1, EPD_MAX_EXPERTS], R = num_ranks with E % R == 0,
  *     N = num_rdma_ranks with R % N == 0, T*k <= INT32_MAX.
@@ -114,9 +113,10 @@ EPD_API size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts
 /*
  * Zero-fills `workspace` (device, `bytes` long) on `stream`. A workspace must
  * be zero-filled once before its first use; the layout call keeps it reusable
- * from then on (its look-back state is tagged with a call counter). A
- * workspace serves one stream at a time: two calls that overlap on the GPU
- * and share a workspace race.
+ * from then on, for calls of any shape that fits (its look-back state words are
+ * tagged with a call counter and a mark no other workspace data carries). A
+ * workspace serves one stream at a time: calls on different streams that
+ * overlap on the GPU and share a workspace race.
  */
 EPD_API epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_stream_t stream);
 
@@ -380,9 +380,13 @@ EPD_API epd_status_t ep_unpermute(const void *expert_out, int64_t capacity_rows,
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - All calls share the one array, which keeps the previous call's contents;
- *     each call clears the counters that must start at zero (on `stream`).
- *     Calls that overlap on the GPU race with each other.
+ *   - All calls share the one array, which keeps the previous call's contents.
+ *     Nothing needs clearing between calls, whatever their shapes: every call
+ *     leaves the tile ticket and finished-block count at zero, and the
+ *     look-back only accepts state words tagged with the running call's
+ *     counter, never an earlier call's ranks, counts or states. Calls in order
+ *     on one stream are safe; calls that overlap on the GPU (other streams)
+ *     race with each other.
  *   - The per-pair ranks it leaves in the shared array are not an input to
  *     ep_permute; a caller running the whole path uses ep_dispatch_layout with
  *     its own workspace.

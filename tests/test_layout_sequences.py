@@ -1,0 +1,218 @@
+"""Layout calls in sequence on one workspace, on the GPU through the C ABI.
+
+"[MoE] Deepseek的All-to-all通信: DeepEP代码解读", section "Dispatch": every
+get_dispatch_layout call computes the layout of its own topk_idx. Here two layout
+calls are issued back to back on one stream and one workspace, with different
+topk_idx and nothing in between, and each call's outputs are compared element by
+element with the oracle -- the counts, masks and offsets, and the second call's
+per-pair ranks through the permute that follows it (output_index, m_indices).
+Sizes span one-wave grids (dsv3: 64 tiles) and grids with more tiles than
+resident blocks (524 288 pairs: 512 tiles).
+
+A second group plants leftovers in the look-back state region of a workspace
+(values an earlier call of another shape, or an earlier call, leaves there) and
+checks that the next call ignores them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import unpermute_ep_dispatch_gb300 as epd
+from unpermute_ep_dispatch_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+E, R, N = 256, 32, 4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from unpermute_ep_dispatch_gb300 import build
+    build.build()
+    epd.load_library()
+
+
+def _case(T, k, seed, routing="uniform"):
+    # 16-column bf16 rows (32 bytes): the permute after the layout reads out the ranks
+    return workloads.make_random_case(T=T, H=16, k=k, E=E, R=R, N=N, dtype="bf16", seed=seed,
+                                      routing=routing, p_invalid=0.05, experts="identity")
+
+
+class Outs:
+    """Device outputs of one layout call (filled with a sentinel first)."""
+
+    def __init__(self, T, dev):
+        self.per_e = torch.full((E,), -7, dtype=torch.int32, device=dev)
+        self.per_r = torch.full((R,), -7, dtype=torch.int32, device=dev)
+        self.per_n = torch.full((N,), -7, dtype=torch.int32, device=dev)
+        self.itr = torch.ones(T, R, dtype=torch.bool, device=dev)
+        self.start = torch.full((E,), -7, dtype=torch.int32, device=dev)
+        self.total = torch.full((1,), -7, dtype=torch.int32, device=dev)
+
+
+def _launch(kind, topk, ws, st, o):
+    if kind == "layout":
+        epd.ep_dispatch_layout(topk, E, R, N, ws, st, tokens_per_expert=o.per_e,
+                               tokens_per_rank=o.per_r, tokens_per_rdma_rank=o.per_n,
+                               is_token_in_rank=o.itr)
+    else:
+        epd.ep_dispatch_layout_offsets(topk, E, R, N, ws, st, tokens_per_expert=o.per_e,
+                                       tokens_per_rank=o.per_r, tokens_per_rdma_rank=o.per_n,
+                                       is_token_in_rank=o.itr, expert_start_loc=o.start,
+                                       total_rows=o.total)
+
+
+def _check_layout(kind, case, o, what):
+    want = oracle.dispatch_layout(case.topk_idx.numpy(), E, R, N)
+    for key, got in (("tokens_per_expert", o.per_e), ("tokens_per_rank", o.per_r),
+                     ("tokens_per_rdma_rank", o.per_n), ("is_token_in_rank", o.itr)):
+        assert np.array_equal(got.cpu().numpy(), want[key]), f"{what}: {key}"
+    if kind == "offsets":
+        start, total = oracle.scan_offsets(want["tokens_per_expert"])
+        assert np.array_equal(o.start.cpu().numpy(), start), f"{what}: expert_start_loc"
+        assert int(o.total.item()) == total, f"{what}: total_rows"
+    return want
+
+
+def _check_ranks(case, ws, st, start, what):
+    """ep_permute_ex over the whole expert range after the layout: its slots are
+    start[e] + the pair ranks the layout left in the workspace."""
+    dev = ws.device
+    x = case.x.to(dev)
+    topk = case.topk_idx.to(dev)
+    out, _, m_idx, out_idx = epd.ep_permute_ex(x, None, topk, E, start, ws, st)
+    torch.cuda.synchronize()
+    want_start, _ = oracle.scan_offsets(
+        oracle.dispatch_layout(case.topk_idx.numpy(), E, R, N)["tokens_per_expert"])
+    want = oracle.permute(case.x.view(torch.uint8).numpy().reshape(case.T, -1), None,
+                          case.topk_idx.numpy(), E, want_start, case.T * case.k)
+    assert np.array_equal(out_idx.cpu().numpy(), want["output_index"]), f"{what}: output_index"
+    assert np.array_equal(m_idx.cpu().numpy(), want["m_indices"]), f"{what}: m_indices"
+
+
+PAIRS = [("layout", "layout"), ("layout", "offsets"), ("offsets", "layout"),
+         ("offsets", "offsets")]
+
+
+@pytest.mark.parametrize("first,second", PAIRS)
+@pytest.mark.parametrize("T,k", [(8192, 8), (65536, 8)])
+def test_two_layout_calls_back_to_back(first, second, T, k):
+    dev = torch.device("cuda")
+    a, b = _case(T, k, seed=T + 1), _case(T, k, seed=T + 2, routing="repeats")
+    ws = epd.new_workspace(T, k, E, R, N, dev)
+    st = epd.new_status(dev)
+    oa, ob = Outs(T, dev), Outs(T, dev)
+    ta, tb = a.topk_idx.to(dev), b.topk_idx.to(dev)
+    torch.cuda.synchronize()
+    for rep in range(3):
+        _launch(first, ta, ws, st, oa)
+        _launch(second, tb, ws, st, ob)        # issued right behind the first, same workspace
+        if second == "layout":
+            epd.ep_scan_offsets(ob.per_e, st, expert_start_loc=ob.start, total_rows=ob.total)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, f"rep {rep}: status {int(st.item())}"
+        _check_layout(first, a, oa, f"rep {rep} first call")
+        _check_layout("offsets", b, ob, f"rep {rep} second call")
+        _check_ranks(b, ws, st, ob.start, f"rep {rep} second call")
+
+
+def test_many_back_to_back_layouts_then_permute():
+    """Twenty layout calls in a row on one workspace, alternating two routings and
+    both entry points; only the last call's ranks reach the permute."""
+    dev = torch.device("cuda")
+    T, k = 16384, 8
+    cases = [_case(T, k, seed=31), _case(T, k, seed=32, routing="repeats")]
+    tops = [c.topk_idx.to(dev) for c in cases]
+    ws = epd.new_workspace(T, k, E, R, N, dev)
+    st = epd.new_status(dev)
+    outs = [Outs(T, dev) for _ in range(20)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        _launch("offsets" if i % 3 else "layout", tops[i % 2], ws, st, o)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for i, o in enumerate(outs):
+        _check_layout("offsets" if i % 3 else "layout", cases[i % 2], o, f"call {i}")
+    last = outs[-1]
+    _check_ranks(cases[1], ws, st, last.start, "last call")
+
+
+def test_lowlatency_large_path_then_layout():
+    """ep_dispatch_lowlatency on a batch beyond its one-kernel form (layout kernel +
+    rectangle permute), then a layout of other routing on the same workspace."""
+    dev = torch.device("cuda")
+    T, k, H = 2048, 8, 128
+    ll = workloads.make_random_case(T=T, H=H, k=k, E=E, R=R, N=N, dtype="bf16", seed=41,
+                                    routing="uniform", experts="identity")
+    b = _case(T, k, seed=42, routing="repeats")
+    ws = epd.new_workspace(T, k, E, R, N, dev)
+    st = epd.new_status(dev)
+    rows = T
+    ob = Outs(T, dev)
+    x = ll.x.to(dev)
+    ta, tb = ll.topk_idx.to(dev), b.topk_idx.to(dev)
+    torch.cuda.synchronize()
+    q, qs, recv, oi, src = epd.ep_dispatch_lowlatency(x, ta, E, R, N, rows, ws, st)
+    _launch("offsets", tb, ws, st, ob)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want_ll = oracle.permute_lowlatency(ll.x.view(torch.int16).numpy().view(np.uint16),
+                                        ll.topk_idx.numpy(), E, rows)
+    assert np.array_equal(recv.cpu().numpy(), want_ll["recv_count"])
+    assert np.array_equal(oi.cpu().numpy(), want_ll["output_index"])
+    _check_layout("offsets", b, ob, "layout after the low-latency dispatch")
+    _check_ranks(b, ws, st, ob.start, "layout after the low-latency dispatch")
+
+
+# ----------------------------------------------------------------------------- leftovers
+def _tile_tokens(k):
+    # tokens per layout tile: 1024 (token, pick) pairs, at most 2048 tokens
+    return max(1, min(2048, 1024 // k)) if k > 0 else 2048
+
+
+def _state_region(T, k):
+    """Byte range of the per-tile look-back state words in a workspace laid out for
+    (T, k, E, R, N): after the 256-byte header block, the T*k pair ranks and the E
+    counts, each region 256-byte aligned; one 64-bit word per tile."""
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    counts_off = up(256 + T * k * 4)
+    state_off = up(counts_off + E * 4)
+    tiles = (T + _tile_tokens(k) - 1) // _tile_tokens(k)
+    return state_off, tiles
+
+
+@pytest.mark.parametrize("plant", ["old_small_tags", "previous_call_tags", "minus_one"])
+def test_leftover_state_words_are_ignored(plant):
+    """A workspace sized for a big layout, a big call first (its pair ranks fill the
+    region where the smaller call keeps its state words), then planted leftovers
+    over the smaller call's state words, then the smaller many-tile call: its
+    counts, offsets and ranks match the oracle."""
+    dev = torch.device("cuda")
+    big = _case(8192, 8, seed=51)
+    small = _case(2048, 8, seed=52, routing="repeats")
+    ws = epd.new_workspace(8192, 8, E, R, N, dev)
+    st = epd.new_status(dev)
+    ob, os_ = Outs(8192, dev), Outs(2048, dev)
+    _launch("offsets", big.topk_idx.to(dev), ws, st, ob)
+    torch.cuda.synchronize()
+    off, tiles = _state_region(2048, 8)
+    assert tiles > 1
+    words = ws[off: off + 8 * tiles].view(torch.int64)
+    epoch = int(ws[8:16].view(torch.int64).item())     # the header's call counter
+    if plant == "old_small_tags":      # 32-bit words an untagged scheme would accept
+        w32 = ws[off: off + 8 * tiles].view(torch.int32)
+        w32.copy_(torch.tensor([5, 6, 9, 10] * (2 * tiles // 4 + 1), dtype=torch.int32)[
+            : 2 * tiles])
+    elif plant == "previous_call_tags":  # states of the call before, marked and published
+        prev = (1 << 63) | ((epoch - 1) << 2) | 1
+        words.fill_(prev - (1 << 64))
+    else:                               # pair ranks of -1 (no selection) everywhere
+        words.fill_(-1)
+    _launch("offsets", small.topk_idx.to(dev), ws, st, os_)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check_layout("offsets", small, os_, f"after planting {plant}")
+    _check_ranks(small, ws, st, os_.start, f"after planting {plant}")

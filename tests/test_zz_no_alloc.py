@@ -93,3 +93,43 @@ def test_noalloc_binding_and_size_limit(lib):
         ctypes.c_void_p(per_e.data_ptr()), ctypes.c_void_p(per_r.data_ptr()), None, None,
         ctypes.c_void_p(st.data_ptr()), None)
     assert rc == epd.EPD_ERR_UNSUPPORTED
+
+
+def test_noalloc_shape_changes_leave_no_stale_state(lib):
+    """The shared array keeps each call's leftovers. A big call writes its pair ranks
+    where a smaller many-tile call keeps its look-back state words; the smaller call
+    must not read them as published states. Repeated, alternating shapes, each
+    result against the oracle."""
+    import numpy as np
+
+    import oracle
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    E, R, N, k = 256, 32, 4, 8
+    shapes = [(8192, 301), (2048, 302), (4096, 303), (1100, 304)]   # (T, seed)
+    cases = [workloads.make_random_case(T=T, H=16, k=k, E=E, R=R, N=N, dtype="bf16", seed=s,
+                                        routing="repeats", p_invalid=0.05, experts="identity")
+             for T, s in shapes]
+    want = [oracle.dispatch_layout(c.topk_idx.numpy(), E, R, N) for c in cases]
+    tops = [c.topk_idx.to(dev) for c in cases]
+    st = epd.new_status(dev)
+    for rep in range(100):
+        outs = []
+        for c, topk in zip(cases, tops):            # four calls back to back, then one sync
+            o = _outputs(c.T, E, R, N, dev, -3)
+            per_e, per_r, per_n, itr = o
+            rc = lib.ep_dispatch_layout_noalloc(
+                ctypes.c_void_p(topk.data_ptr()), c.T, k, E, R, N,
+                ctypes.c_void_p(per_e.data_ptr()), ctypes.c_void_p(per_r.data_ptr()),
+                ctypes.c_void_p(per_n.data_ptr()), ctypes.c_void_p(itr.data_ptr()),
+                ctypes.c_void_p(st.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+            assert rc == epd.EPD_OK
+            outs.append(o)
+        torch.cuda.synchronize(dev)
+        assert int(st.item()) == 0, f"rep {rep}: status {int(st.item())}"
+        for c, w, (per_e, per_r, per_n, itr) in zip(cases, want, outs):
+            what = f"rep {rep} T={c.T}"
+            assert np.array_equal(per_e.cpu().numpy(), w["tokens_per_expert"]), what
+            assert np.array_equal(per_r.cpu().numpy(), w["tokens_per_rank"]), what
+            assert np.array_equal(per_n.cpu().numpy(), w["tokens_per_rdma_rank"]), what
+            assert np.array_equal(itr.cpu().numpy(), w["is_token_in_rank"]), what

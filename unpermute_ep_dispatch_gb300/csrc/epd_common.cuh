@@ -17,13 +17,14 @@ namespace epd {
 // at fixed offsets that depend on T*k only, so ep_permute (which is not given
 // R and N) finds them; the look-back state follows.
 struct WsHeader {
-    uint32_t ticket;       // next token tile to hand out (dynamic tile order)
-    uint32_t done;         // number of layout blocks that finished this call
-    uint32_t epoch;        // call counter; look-back states carry it
+    uint32_t ticket;       // next token tile to hand out (dynamic tile order); wraps to 0
+                           // by itself once a call has handed out all its tiles
+    uint32_t done;         // layout blocks of the running call that finished; wraps to 0
+    uint64_t epoch;        // call counter; look-back states carry it
     int32_t total_pairs;   // P of the last layout call
     int32_t num_tokens;    // T of the last layout call
     int32_t num_topk;      // k of the last layout call
-    uint32_t pad[10];
+    uint32_t pad[9];
 };
 static_assert(sizeof(WsHeader) == 64, "header is one 64-byte block");
 
@@ -68,7 +69,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N)
     w.pair_rank_off = ws_pair_rank_off();
     w.counts_off = ws_counts_off(T, k);
     w.state_off = align_up(w.counts_off + (size_t)E * 4, kAlign);
-    w.agg_off = align_up(w.state_off + (size_t)w.tiles * 4, kAlign);
+    w.agg_off = align_up(w.state_off + (size_t)w.tiles * 8, kAlign);  // 64-bit state words
     w.incl_off = align_up(w.agg_off + (size_t)w.tiles * w.cols_pad * 4, kAlign);
     w.total = align_up(w.incl_off + (size_t)w.tiles * w.cols_pad * 4, kAlign);
     return w;
@@ -168,6 +169,22 @@ __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint64_t *p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 

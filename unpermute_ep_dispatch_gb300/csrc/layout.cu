@@ -37,6 +37,12 @@
 namespace epd {
 namespace {
 
+// A tile's 64-bit state word is kStateMark | call counter << 2 | flag. Nothing else
+// the library writes into a workspace has the top bit of a 64-bit word set (every
+// other int32 there is >= -1, and two -1 words would need a call counter of 2^61),
+// so leftovers of a call of another shape -- pair ranks, counts -- or of an
+// earlier call never read as a published state.
+constexpr uint64_t kStateMark = 1ull << 63;
 constexpr uint32_t kStateAgg = 1;   // tile published its own counts
 constexpr uint32_t kStateIncl = 2;  // tile published counts of itself and all earlier tiles
 constexpr uint32_t kDefaultSpinLimit = 1u << 19;  // polls with back-off: about a second
@@ -49,7 +55,7 @@ struct LayoutArgs {
     WsHeader *hdr;
     int32_t *pair_rank;
     int32_t *ws_counts;
-    uint32_t *state;
+    uint64_t *state;
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
     int id_bits;  // bits needed for an expert id in [0, E)
@@ -84,7 +90,7 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     int *node_of = rank_of + a.E;          // [R] simulated node of each rank
     int16_t *s_pick = reinterpret_cast<int16_t *>(node_of + a.E);  // [tile pairs] expert or -1
     __shared__ int s_tile;
-    __shared__ uint32_t s_epoch;
+    __shared__ uint64_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
     __shared__ int s_red[W], s_red2[W];
 
@@ -96,21 +102,21 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     }
     for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
     for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
-    // The ticket and the call counter are left by the previous call on this workspace,
-    // which has completed once the kernel before this one on the stream has started;
-    // topk_idx may come from that kernel, so it is read only after the wait. A call
-    // with one tile needs neither (no look-back, nothing to reset).
+    // The tile ticket is taken before the dependency wait. It wraps to 0 by itself once
+    // all `tiles` tickets of a call are handed out, and the next kernel on the stream
+    // can only start once every block of this one has taken its ticket (the trigger
+    // below follows it), so a layout call issued right after this one -- on the same
+    // workspace -- starts from ticket 0 whatever the timing. Everything else the call
+    // reads from the workspace (the call counter, the look-back state) and topk_idx
+    // (which the kernel before may write) is read after the wait, when every earlier
+    // call has completed. A call with one tile needs none of it (no look-back).
     const bool multi = a.tiles > 1;
-    if (tid == 0) {
-        s_tile = multi ? (int)atomicAdd(&a.hdr->ticket, 1u) : 0;
-        s_epoch = multi ? ld_relaxed_gpu(&a.hdr->epoch) : 0u;
-    }
+    if (tid == 0) s_tile = multi ? (int)atomicInc(&a.hdr->ticket, (unsigned)(a.tiles - 1)) : 0;
+    __syncthreads();
     pdl_wait();
     pdl_trigger();
-    __syncthreads();
+    if (tid == 0) s_epoch = multi ? ld_relaxed_gpu(&a.hdr->epoch) : 0ull;
     const int tile = s_tile;
-    const uint32_t epoch = s_epoch;
-    const uint32_t tag = epoch << 2;
     const int t0 = tile * a.tile_tokens;
     const int ntok = max(0, min(a.tile_tokens, a.T - t0));
     const int npairs = ntok * a.k;
@@ -243,6 +249,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // prefix). The block barrier orders every thread's stores before thread 0's
     // release store of the state word.
     const bool publish = multi && tile != a.stalled_tile;
+    const uint64_t epoch = s_epoch;  // written by thread 0 before the barriers above
+    const uint64_t tag = kStateMark | (epoch << 2);
     int32_t *my_agg = a.agg + (size_t)tile * a.cols_pad;
     int32_t *my_incl = a.incl + (size_t)tile * a.cols_pad;
     if (multi) {
@@ -300,8 +308,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
                 while (true) {
                     uint32_t st = kStateIncl;  // before tile 0: an empty inclusive prefix
                     if (idx >= 0) {
-                        const uint32_t v = ld_acquire_gpu(&a.state[idx]);
-                        st = ((v & ~3u) == tag) ? (v & 3u) : 0u;
+                        const uint64_t v = ld_acquire_gpu(&a.state[idx]);
+                        st = ((v & ~3ull) == tag) ? (uint32_t)(v & 3ull) : 0u;
                     }
                     const uint32_t incl_mask = __ballot_sync(0xffffffffu, st == kStateIncl);
                     const uint32_t wait_mask = __ballot_sync(0xffffffffu, st == 0);
@@ -434,13 +442,13 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         }
     }
 
-    // (9) the last block to finish resets the call state for the next call
+    // (9) the last block to finish advances the call counter for the next call (which
+    // reads it only after its dependency wait, once this call has completed); the
+    // finished-block count wraps back to 0 by itself
     __syncthreads();
     if (tid == 0 && multi) {
-        const unsigned prev = atomicAdd(&a.hdr->done, 1u);
+        const unsigned prev = atomicInc(&a.hdr->done, (unsigned)(a.tiles - 1));
         if (prev == (unsigned)a.tiles - 1) {
-            a.hdr->done = 0;
-            a.hdr->ticket = 0;
             a.hdr->epoch = epoch + 1;
             __threadfence();
         }
@@ -508,7 +516,7 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     a.hdr = reinterpret_cast<WsHeader *>(ws + w.header_off);
     a.pair_rank = reinterpret_cast<int32_t *>(ws + w.pair_rank_off);
     a.ws_counts = reinterpret_cast<int32_t *>(ws + w.counts_off);
-    a.state = reinterpret_cast<uint32_t *>(ws + w.state_off);
+    a.state = reinterpret_cast<uint64_t *>(ws + w.state_off);
     a.agg = reinterpret_cast<int32_t *>(ws + w.agg_off);
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
     a.tiles = w.tiles;
@@ -701,11 +709,11 @@ extern "C" epd_status_t ep_dispatch_layout_noalloc(const int64_t *topk_idx, int 
     void *scratch = nullptr;
     const epd_status_t st = noalloc_scratch_address(&scratch);
     if (st != EPD_OK) return st;
+    // Nothing is cleared between calls: every call leaves the tile ticket and the
+    // finished-block count at zero, and the look-back only accepts state words tagged
+    // with the running call's counter, so the leftovers of an earlier call of any shape
+    // (ranks, counts, older states) in the shared array are never read as published.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The tile ticket and the finished-block count must start at zero; the call
-    // counter that tags the look-back state carries over from the previous call.
-    if (cudaMemsetAsync(scratch, 0, offsetof(WsHeader, epoch), s) != cudaSuccess)
-        return record_cuda_error();
     return layout_launch(nullptr, nullptr, 1, topk_idx, T, k, num_experts, num_ranks, num_rdma_ranks,
                          tokens_per_expert, tokens_per_rank, tokens_per_rdma_rank,
                          is_token_in_rank, scratch, status, -1, kDefaultSpinLimit, s);
