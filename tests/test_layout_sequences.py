@@ -191,14 +191,18 @@ def test_leftover_state_words_are_ignored(plant):
     over the smaller call's state words, then the smaller many-tile call: its
     counts, offsets and ranks match the oracle."""
     dev = torch.device("cuda")
-    big = _case(8192, 8, seed=51)
-    small = _case(2048, 8, seed=52, routing="repeats")
-    ws = epd.new_workspace(8192, 8, E, R, N, dev)
+    # batches beyond one thread-block cluster (more than 131 072 pairs at E = 256): both
+    # calls run the tile form, whose look-back reads the state words
+    TB, TS = 32768, 20000
+    big = _case(TB, 8, seed=51)
+    small = _case(TS, 8, seed=52, routing="repeats")
+    ws = epd.new_workspace(TB, 8, E, R, N, dev)
     st = epd.new_status(dev)
-    ob, os_ = Outs(8192, dev), Outs(2048, dev)
+    ob, os_ = Outs(TB, dev), Outs(TS, dev)
     _launch("offsets", big.topk_idx.to(dev), ws, st, ob)
     torch.cuda.synchronize()
-    off, tiles = _state_region(2048, 8)
+    off, tiles = _state_region(TS, 8)
+    assert off + 8 * tiles <= 256 + TB * 8 * 4     # inside the big call's pair ranks
     assert tiles > 1
     words = ws[off: off + 8 * tiles].view(torch.int64)
     epoch = int(ws[8:16].view(torch.int64).item())     # the header's call counter
@@ -207,12 +211,14 @@ def test_leftover_state_words_are_ignored(plant):
         w32.copy_(torch.tensor([5, 6, 9, 10] * (2 * tiles // 4 + 1), dtype=torch.int32)[
             : 2 * tiles])
     elif plant == "previous_call_tags":  # states of the call before, marked and published
-        prev = (1 << 63) | ((epoch - 1) << 2) | 1
-        words.fill_(prev - (1 << 64))
+        assert epoch >= 1
+        prev = (1 << 63) | (((epoch - 1) & ((1 << 61) - 1)) << 2) | 1
+        words.fill_(prev - (1 << 64))               # the same 64 bits as a signed value
     else:                               # pair ranks of -1 (no selection) everywhere
         words.fill_(-1)
     _launch("offsets", small.topk_idx.to(dev), ws, st, os_)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+    assert int(ws[8:16].view(torch.int64).item()) == epoch + 1   # the tile form ran
     _check_layout("offsets", small, os_, f"after planting {plant}")
     _check_ranks(small, ws, st, os_.start, f"after planting {plant}")

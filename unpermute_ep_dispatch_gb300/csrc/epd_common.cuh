@@ -123,6 +123,28 @@ inline epd_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, si
     return record_cuda_error();
 }
 
+// The same with the grid cut into thread-block clusters of `cluster` blocks.
+template <typename... KArgs, typename... Args>
+inline epd_status_t launch_pdl_cluster(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                                       int cluster, cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return record_cuda_error();
+}
+
 // Resident blocks of `kernel` per SM at `block` threads and `smem` dynamic bytes.
 template <typename K>
 inline int blocks_per_sm(K kernel, int block, size_t smem) {
@@ -200,6 +222,41 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
 __device__ __forceinline__ void st16(void *p, const uint4 &v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------- thread-block clusters
+// Rank of this block inside its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Split cluster barrier: every thread of every block of the cluster arrives (its
+// earlier writes, shared memory of other blocks included, are released) and later
+// waits (acquiring what the others released). Called by all threads, uniformly.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory variable in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+    return r;
+}
+
+// 16-byte store to another block's shared memory (an address from cluster_map).
+__device__ __forceinline__ void cluster_st_v4(uint32_t addr, const int4 &v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
 

@@ -46,6 +46,8 @@ constexpr uint64_t kStateMark = 1ull << 63;
 constexpr uint32_t kStateAgg = 1;   // tile published its own counts
 constexpr uint32_t kStateIncl = 2;  // tile published counts of itself and all earlier tiles
 constexpr uint32_t kDefaultSpinLimit = 1u << 19;  // polls with back-off: about a second
+constexpr int kMaxIdBits = 12;                     // an expert id below EPD_MAX_EXPERTS
+static_assert((1 << kMaxIdBits) >= EPD_MAX_EXPERTS, "expert ids fit kMaxIdBits bits");
 
 struct LayoutArgs {
     const int64_t *topk;
@@ -59,6 +61,7 @@ struct LayoutArgs {
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
     int id_bits;  // bits needed for an expert id in [0, E)
+    int rank_shift, node_shift;  // log2(E/R), log2(R/N) when powers of two, else -1
     int32_t *start_out;  // optional: expert offsets written by the last tile (fused step 2)
     int32_t *total_out;
     int alignment;
@@ -73,22 +76,54 @@ __device__ __forceinline__ int warp_sum(int v) {
     return v;
 }
 
-template <int W>
+// kChunks: 32-pair chunks per warp at most (a tile holds up to W * 32 * kChunks pairs).
+// kCluster: the tiles are the blocks of one thread-block cluster, all running at
+// once; each block pushes its counts into the shared memory of every later block
+// of the cluster and one cluster barrier completes every prefix (no ticket, no
+// look-back through global memory). Otherwise tiles are handed out by ticket and
+// chained by the decoupled look-back.
+// Byte offsets of the layout kernel's shared-memory regions; every region that is
+// read or written with 16-byte vectors starts on a 16-byte boundary.
+struct LayoutSmem {
+    size_t rmask, nmask, hist, agg, excl, rank_of, node_of, pick, stage, total;
+};
+
+__host__ __device__ inline LayoutSmem layout_smem(int E, int W, int cols_pad, int tile_tokens,
+                                                  int64_t tile_pairs, int stage_rows) {
+    LayoutSmem m;
+    m.rmask = 0;
+    m.nmask = m.rmask + (size_t)tile_tokens * 8;
+    m.hist = m.nmask + (size_t)tile_tokens * 8;
+    m.agg = align_up(m.hist + (size_t)W * (E + 1) * 4, 16);
+    m.excl = m.agg + (size_t)cols_pad * 4;
+    m.rank_of = m.excl + (size_t)cols_pad * 4;
+    m.node_of = m.rank_of + (size_t)E * 4;
+    m.pick = align_up(m.node_of + (size_t)E * 4, 16);
+    m.stage = align_up(m.pick + (size_t)tile_pairs * 2, 16);
+    m.total = m.stage + (size_t)stage_rows * cols_pad * 4;
+    return m;
+}
+
+template <int W, int kChunks, bool kCluster>
 __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
-    constexpr int kChunks = kLayoutTilePairs / kThreads;  // 32-pair chunks per warp
     extern __shared__ int4 smem_raw[];
-    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(smem_raw);  // ranks
-    unsigned long long *tok_nmask = tok_rmask + kLayoutMaxTileTokens;                 // nodes
+    char *sm = reinterpret_cast<char *>(smem_raw);
+    const LayoutSmem L = layout_smem(a.E, W, a.cols_pad, a.tile_tokens,
+                                     (int64_t)a.tile_tokens * a.k, 0);
+    unsigned long long *tok_rmask = reinterpret_cast<unsigned long long *>(sm + L.rmask);  // ranks
+    unsigned long long *tok_nmask = reinterpret_cast<unsigned long long *>(sm + L.nmask);  // nodes
     // [W][E + 1] warp histograms -> warp bases; rows padded by one word so that the
     // per-expert scan across warps (stride of one row) hits 32 different banks
     const int hws = a.E + 1;
-    int *hw = reinterpret_cast<int *>(tok_nmask + kLayoutMaxTileTokens);
-    int *col_agg = hw + W * hws;           // [cols_pad] this tile's counts
-    int *col_excl = col_agg + a.cols_pad;  // [cols_pad] counts of earlier tiles
-    int *rank_of = col_excl + a.cols_pad;  // [E] simulated rank of each expert
-    int *node_of = rank_of + a.E;          // [R] simulated node of each rank
-    int16_t *s_pick = reinterpret_cast<int16_t *>(node_of + a.E);  // [tile pairs] expert or -1
+    int *hw = reinterpret_cast<int *>(sm + L.hist);
+    int *col_agg = reinterpret_cast<int *>(sm + L.agg);    // [cols_pad] this tile's counts
+    int *col_excl = reinterpret_cast<int *>(sm + L.excl);  // [cols_pad] counts of earlier tiles
+    int *rank_of = reinterpret_cast<int *>(sm + L.rank_of);  // [E] simulated rank of each expert
+    int *node_of = reinterpret_cast<int *>(sm + L.node_of);  // [R] simulated node of each rank
+    int16_t *s_pick = reinterpret_cast<int16_t *>(sm + L.pick);  // [tile pairs] expert or -1
+    // cluster: [tiles][cols_pad] counts of the earlier blocks, sent by each of them
+    int *s_stage = reinterpret_cast<int *>(sm + L.stage);
     __shared__ int s_tile;
     __shared__ uint64_t s_epoch;
     __shared__ int s_win_aggs, s_win_incl, s_win_done;
@@ -102,6 +137,9 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     }
     for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
     for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
+    // cluster: this block has started; the other blocks store into its shared memory
+    // only once every block has arrived here
+    if constexpr (kCluster) cluster_arrive_release();
     // The tile ticket is taken before the dependency wait. It wraps to 0 by itself once
     // all `tiles` tickets of a call are handed out, and the next kernel on the stream
     // can only start once every block of this one has taken its ticket (the trigger
@@ -110,8 +148,10 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // reads from the workspace (the call counter, the look-back state) and topk_idx
     // (which the kernel before may write) is read after the wait, when every earlier
     // call has completed. A call with one tile needs none of it (no look-back).
-    const bool multi = a.tiles > 1;
-    if (tid == 0) s_tile = multi ? (int)atomicInc(&a.hdr->ticket, (unsigned)(a.tiles - 1)) : 0;
+    const bool multi = !kCluster && a.tiles > 1;  // ticket, look-back and call counter
+    if (tid == 0)
+        s_tile = kCluster ? (int)cluster_ctarank()
+                          : multi ? (int)atomicInc(&a.hdr->ticket, (unsigned)(a.tiles - 1)) : 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
@@ -155,17 +195,20 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         if (c >= live) continue;
         const int e = pe[c];
         uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
-        for (int b = 0; b < a.id_bits; ++b) {
-            const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
-            peers &= ((e >> b) & 1) ? set : ~set;
+#pragma unroll
+        for (int b = 0; b < kMaxIdBits; ++b) {
+            if (b < a.id_bits) {  // the same for every lane
+                const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
+                peers &= ((e >> b) & 1) ? set : ~set;
+            }
         }
-        if (e >= 0) {
-            const int before = __popc(peers & lanemask_lt());
-            const int base = my_hist[e];
-            pr[c] = base + before;
-            __syncwarp(peers);
-            if (before == 0) my_hist[e] = base + __popc(peers);
-        }
+        // every lane reads its group's count before the group's lowest lane adds to it;
+        // the warp stays converged (whole-warp syncs only)
+        const int before = __popc(peers & lanemask_lt());
+        const int base = e >= 0 ? my_hist[e] : 0;
+        pr[c] = base + before;
+        __syncwarp();
+        if (e >= 0 && before == 0) my_hist[e] = base + __popc(peers);
         __syncwarp();
     }
 
@@ -206,8 +249,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
             for (int j = 0; j < a.k; ++j) {
                 const int e = row[j];
                 if (e < 0) continue;
-                const int r = rank_of[e];
-                const int n = node_of[r];
+                const int r = a.rank_shift >= 0 ? e >> a.rank_shift : rank_of[e];
+                const int n = a.node_shift >= 0 ? r >> a.node_shift : node_of[r];
                 if (small_r) rm |= 1ull << r;
                 if (small_n) nm |= 1ull << n;
                 if (!small_r || !small_n) {
@@ -244,6 +287,32 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         }
     }
     __syncthreads();
+
+    if constexpr (kCluster) {
+        // (4') every block of the cluster has started: send this tile's counts, as 16-byte
+        // vectors, into row `tile` of the staging area of every later block -- the expert
+        // columns to each of them, all columns to the last one (which writes the totals)
+        cluster_wait_acquire();
+        const int later = a.tiles - 1 - tile;
+        const int nv_e = (a.E + 3) >> 2, nv_all = a.cols_pad >> 2;
+        const int n_mid = later > 0 ? (later - 1) * nv_e : 0;
+        const int n_send = later > 0 ? n_mid + nv_all : 0;
+        const int4 *row = reinterpret_cast<const int4 *>(col_agg);
+        int *dst_row = s_stage + tile * a.cols_pad;
+        for (int i = tid; i < n_send; i += kThreads) {
+            int d, v;
+            if (i < n_mid) {
+                d = i / nv_e;
+                v = i - d * nv_e;
+                d += tile + 1;
+            } else {
+                d = a.tiles - 1;
+                v = i - n_mid;
+            }
+            cluster_st_v4(cluster_map(dst_row + 4 * v, (uint32_t)d), row[v]);
+        }
+        cluster_arrive_release();
+    }
 
     // (4) publish this tile's counts (tile 0 has no predecessor: its counts are its
     // prefix). The block barrier orders every thread's stores before thread 0's
@@ -296,8 +365,22 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         }
     }
 
+    // cluster: the barrier completes once every block's rows have landed, and no block
+    // touches another's shared memory after it (so any block may exit); the prefix of
+    // this tile is the sum of the rows of the earlier tiles
+    if constexpr (kCluster) {
+        cluster_wait_acquire();
+        const int ncol = tile == a.tiles - 1 ? a.cols : a.E;
+        for (int c = tid; c < ncol; c += kThreads) {
+            int sum = 0;
+            for (int t = 0; t < tile; ++t) sum += s_stage[t * a.cols_pad + c];
+            col_excl[c] = sum;
+        }
+        __syncthreads();
+    }
+
     // (5) decoupled look-back over earlier tiles
-    if (tile > 0) {
+    if (multi && tile > 0) {
         int pos = tile - 1;
         while (true) {
             if (warp == 0) {
@@ -455,31 +538,149 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     }
 }
 
-size_t layout_smem_bytes(int E, int cols_pad) {
-    return 2 * (size_t)kLayoutMaxTileTokens * sizeof(unsigned long long) +
-           ((size_t)layout_warps(E) * (E + 1) + 2 * (size_t)cols_pad + 2 * (size_t)E) * sizeof(int) +
-           (size_t)kLayoutTilePairs * sizeof(int16_t);
+size_t layout_smem_bytes(int E, int cols_pad, int tile_tokens, int64_t tile_pairs,
+                         int stage_rows) {
+    return layout_smem(E, layout_warps(E), cols_pad, tile_tokens, tile_pairs, stage_rows).total;
+}
+
+constexpr int kMaxCluster = 16;         // blocks of the cluster form (non-portable above 8)
+constexpr int kClusterMaxChunks = 8;    // 32-pair chunks per warp in the cluster form
+
+// Raises the kernel's dynamic shared-memory limit to `smem` if needed (per device).
+template <typename K>
+epd_status_t opt_in_smem(K kernel, size_t smem) {
+    if (smem <= 48 * 1024) return EPD_OK;
+    // the opt-in limit covers static and dynamic shared memory together
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
+        return record_cuda_error();
+    if (smem + fa.sharedSizeBytes > (size_t)optin) return EPD_ERR_UNSUPPORTED;
+    if ((int)smem > fa.maxDynamicSharedSizeBytes &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return record_cuda_error();
+    return EPD_OK;
+}
+
+template <int W, int CH>
+epd_status_t launch_tiles(const LayoutArgs &a, size_t smem, cudaStream_t stream) {
+    auto kernel = layout_kernel<W, CH, false>;
+    const epd_status_t st = opt_in_smem(kernel, smem);
+    if (st != EPD_OK) return st;
+    return launch_pdl(kernel, a.tiles, W * 32, smem, stream, a);
+}
+
+// Whether a cluster of C blocks of layout_kernel<W, CH, true> with `smem` bytes each can
+// run on the current device (the answer for the last size asked is kept per device).
+template <int W, int CH>
+bool cluster_fits(int C, size_t smem) {
+    static std::atomic<unsigned long long> last[64][2];  // (smem << 1 | fits) + 1, 0 = unknown
+    auto kernel = layout_kernel<W, CH, true>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const int slot = C > 8 ? 1 : 0;
+    std::atomic<unsigned long long> *cache =
+        (dev >= 0 && dev < 64) ? &last[dev][slot] : nullptr;
+    if (cache) {
+        const unsigned long long v = cache->load(std::memory_order_acquire);
+        if (v != 0 && ((v - 1) >> 1) == smem) return ((v - 1) & 1) != 0;
+    }
+    bool fits = opt_in_smem(kernel, smem) == EPD_OK;
+    if (fits && C > 8 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        fits = false;
+    }
+    if (fits) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)C);
+        cfg.blockDim = dim3((unsigned)(W * 32));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        fits = n >= 1;
+    }
+    if (cache) cache->store(((unsigned long long)smem << 1 | (fits ? 1ull : 0ull)) + 1,
+                            std::memory_order_release);
+    return fits;
+}
+
+template <int W, int CH>
+epd_status_t launch_cluster(const LayoutArgs &a, size_t smem, cudaStream_t stream) {
+    return launch_pdl_cluster(layout_kernel<W, CH, true>, a.tiles, W * 32, smem, a.tiles, stream,
+                              a);
 }
 
 template <int W>
-epd_status_t launch_layout(const LayoutArgs &a, size_t smem, cudaStream_t stream) {
-    auto kernel = layout_kernel<W>;
-    if (smem > 48 * 1024) {
-        // the opt-in limit covers static and dynamic shared memory together
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-                cudaSuccess ||
-            cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
-            return record_cuda_error();
-        if (smem + fa.sharedSizeBytes > (size_t)optin) return EPD_ERR_UNSUPPORTED;
-        if ((int)smem > fa.maxDynamicSharedSizeBytes &&
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-                cudaSuccess)
-            return record_cuda_error();
+bool cluster_fits_any(int CH, int C, size_t smem) {
+    switch (CH) {
+        case 1: return cluster_fits<W, 1>(C, smem);
+        case 2: return cluster_fits<W, 2>(C, smem);
+        case 4: return cluster_fits<W, 4>(C, smem);
+        default: return cluster_fits<W, 8>(C, smem);
     }
-    return launch_pdl(kernel, a.tiles, W * 32, smem, stream, a);
+}
+
+template <int W>
+epd_status_t launch_cluster_any(int CH, const LayoutArgs &a, size_t smem, cudaStream_t stream) {
+    switch (CH) {
+        case 1: return launch_cluster<W, 1>(a, smem, stream);
+        case 2: return launch_cluster<W, 2>(a, smem, stream);
+        case 4: return launch_cluster<W, 4>(a, smem, stream);
+        default: return launch_cluster<W, 8>(a, smem, stream);
+    }
+}
+
+// The cluster form for a batch of `pairs` (token, pick) pairs: the number of blocks
+// (a power of two, 2..16, about one per 1024 pairs) and the chunks per warp, or
+// C = 0 when the batch fits one tile, exceeds what one cluster holds, or the device
+// cannot co-schedule the cluster.
+struct ClusterPlan {
+    int C, chunks, tile_tokens;
+    size_t smem;
+};
+
+ClusterPlan plan_cluster(int T, int k, int E, int cols_pad) {
+    ClusterPlan p = {0, 0, 0, 0};
+    const int W = layout_warps(E);
+    const int64_t pairs = (int64_t)T * k;
+    if (W < 16 || pairs <= kLayoutTilePairs) return p;
+    int C = 2;
+    while (C < kMaxCluster && (int64_t)C * kLayoutTilePairs < pairs) C *= 2;
+    for (; C >= 2; C /= 2) {
+        const int tt = (T + C - 1) / C;
+        const int64_t tp = (int64_t)tt * k;
+        if (tt > kLayoutMaxTileTokens || tp > (int64_t)W * 32 * kClusterMaxChunks) return p;
+        int ch = 1;
+        while ((int64_t)ch * W * 32 < tp) ch *= 2;
+        const size_t smem = layout_smem_bytes(E, cols_pad, tt, tp, C);
+        const bool fits = W == 32 ? cluster_fits_any<32>(ch, C, smem)
+                                  : cluster_fits_any<16>(ch, C, smem);
+        if (fits) {
+            p.C = C;
+            p.chunks = ch;
+            p.tile_tokens = tt;
+            p.smem = smem;
+            return p;
+        }
+    }
+    return p;
 }
 
 epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment,
@@ -498,7 +699,6 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     if (spin_limit == 0) return EPD_ERR_INVALID_ARG;
 
     const WsLayout w = ws_layout(T, k, E, R, N);
-    const size_t smem = layout_smem_bytes(E, w.cols_pad);
     char *ws = static_cast<char *>(workspace);
     LayoutArgs a;
     a.topk = topk_idx;
@@ -526,16 +726,34 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     a.alignment = alignment;
     a.id_bits = 0;
     while ((1 << a.id_bits) < E) ++a.id_bits;
+    auto log2_exact = [](int v) {
+        int b = 0;
+        while ((1 << b) < v) ++b;
+        return (1 << b) == v ? b : -1;
+    };
+    a.rank_shift = log2_exact(a.epr);
+    a.node_shift = log2_exact(a.rpn);
     a.cols = w.cols;
     a.cols_pad = w.cols_pad;
     a.status = status;
     a.stalled_tile = stalled_tile;
     a.spin_limit = spin_limit;
-    switch (layout_warps(E)) {
-        case 32: return launch_layout<32>(a, smem, stream);
-        case 16: return launch_layout<16>(a, smem, stream);
-        case 8: return launch_layout<8>(a, smem, stream);
-        default: return launch_layout<4>(a, smem, stream);
+    // the failure-detection hook needs the look-back, so it always runs the tile form
+    const ClusterPlan cp = stalled_tile < 0 ? plan_cluster(T, k, E, w.cols_pad)
+                                            : ClusterPlan{0, 0, 0, 0};
+    if (cp.C > 0) {
+        a.tiles = cp.C;
+        a.tile_tokens = cp.tile_tokens;
+        return layout_warps(E) == 32 ? launch_cluster_any<32>(cp.chunks, a, cp.smem, stream)
+                                     : launch_cluster_any<16>(cp.chunks, a, cp.smem, stream);
+    }
+    const size_t smem = layout_smem_bytes(E, w.cols_pad, a.tile_tokens,
+                                          (int64_t)a.tile_tokens * k, 0);
+    switch (layout_warps(E)) {  // one 1024-pair tile per block
+        case 32: return launch_tiles<32, 1>(a, smem, stream);
+        case 16: return launch_tiles<16, 2>(a, smem, stream);
+        case 8: return launch_tiles<8, 4>(a, smem, stream);
+        default: return launch_tiles<4, 8>(a, smem, stream);
     }
 }
 
