@@ -46,8 +46,7 @@ constexpr uint64_t kStateMark = 1ull << 63;
 constexpr uint32_t kStateAgg = 1;   // tile published its own counts
 constexpr uint32_t kStateIncl = 2;  // tile published counts of itself and all earlier tiles
 constexpr uint32_t kDefaultSpinLimit = 1u << 19;  // polls with back-off: about a second
-constexpr int kMaxIdBits = 12;                     // an expert id below EPD_MAX_EXPERTS
-static_assert((1 << kMaxIdBits) >= EPD_MAX_EXPERTS, "expert ids fit kMaxIdBits bits");
+static_assert(EPD_MAX_EXPERTS <= 4096, "expert ids fit the 12 bits the narrowest block ranks");
 
 struct LayoutArgs {
     const int64_t *topk;
@@ -60,7 +59,6 @@ struct LayoutArgs {
     uint64_t *state;
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
-    int id_bits;  // bits needed for an expert id in [0, E)
     int rank_shift, node_shift;  // log2(E/R), log2(R/N) when powers of two, else -1
     int32_t *start_out;  // optional: expert offsets written by the last tile (fused step 2)
     int32_t *total_out;
@@ -104,9 +102,31 @@ __host__ __device__ inline LayoutSmem layout_smem(int E, int W, int cols_pad, in
     return m;
 }
 
+// Lane b gets the number of lanes of the warp whose word x has bit b set: the warp's
+// 32 x 32 bit matrix is transposed by five butterfly exchanges of half-blocks, and
+// each lane then counts the bits of its row.
+__device__ __forceinline__ int bit_column_count(uint32_t x, int lane) {
+#pragma unroll
+    for (int j = 16; j >= 1; j >>= 1) {
+        const uint32_t m = j == 16 ? 0x0000ffffu
+                         : j == 8  ? 0x00ff00ffu
+                         : j == 4  ? 0x0f0f0f0fu
+                         : j == 2  ? 0x33333333u
+                                   : 0x55555555u;
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y & m) << j));
+    }
+    return __popc(x);
+}
+
+// The low four bits of b spread to the four bytes of a word (byte i = bit i).
+__device__ __forceinline__ int spread4(uint32_t b) { return (int)(((b & 0xFu) * 0x00204081u) & 0x01010101u); }
+
 template <int W, int kChunks, bool kCluster>
 __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
+    // bits of the largest expert id this block width serves (layout_warps)
+    constexpr int kIdBits = W >= 32 ? 9 : W >= 16 ? 10 : W >= 8 ? 11 : 12;
     extern __shared__ int4 smem_raw[];
     char *sm = reinterpret_cast<char *>(smem_raw);
     const LayoutSmem L = layout_smem(a.E, W, a.cols_pad, a.tile_tokens,
@@ -130,7 +150,12 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     __shared__ int s_red[W], s_red2[W];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < W * hws; i += kThreads) hw[i] = 0;
+    {  // zero the warp histograms, 16 bytes per store (the region is 16-byte aligned)
+        const int n4 = (W * hws) >> 2;
+        int4 *hw4 = reinterpret_cast<int4 *>(hw);
+        for (int i = tid; i < n4; i += kThreads) hw4[i] = make_int4(0, 0, 0, 0);
+        for (int i = 4 * n4 + tid; i < W * hws; i += kThreads) hw[i] = 0;
+    }
     for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
@@ -195,12 +220,12 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         if (c >= live) continue;
         const int e = pe[c];
         uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
+        // one ballot per bit of the largest id a block of this width serves (bits above
+        // the highest bit of E - 1 are 0 for every valid lane: they change nothing)
 #pragma unroll
-        for (int b = 0; b < kMaxIdBits; ++b) {
-            if (b < a.id_bits) {  // the same for every lane
-                const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
-                peers &= ((e >> b) & 1) ? set : ~set;
-            }
+        for (int b = 0; b < kIdBits; ++b) {
+            const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
+            peers &= ((e >> b) & 1) ? set : ~set;
         }
         // every lane reads its group's count before the group's lowest lane adds to it;
         // the warp stays converged (whole-warp syncs only)
@@ -237,9 +262,9 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // (3) one lane per token, warps taken from the top so that they run beside the
     // scan above: the ranks and nodes the token reaches (read from its picks in
     // shared memory), as bit masks when R, N <= 64 (a token counts once per rank and
-    // once per node), and the tile's tokens per rank and per node from one ballot
-    // per mask bit; for R or N above 64 each token counts its distinct ranks or
-    // nodes by comparing its picks
+    // once per node), and the tile's tokens per rank and per node by counting the
+    // columns of the warp's masks; for R or N above 64 each token counts its distinct
+    // ranks or nodes by comparing its picks
     const bool small_r = a.R <= 64, small_n = a.N <= 64;
     for (int base = (W - 1 - warp) * 32; base < ntok; base += kThreads) {
         const int tl = base + lane;
@@ -271,19 +296,14 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         }
         // lane b of group g ends up with the warp's count for bit 32 g + b
         for (int g = 0; g < 2; ++g) {
-            const int nb_r = small_r ? min(32, a.R - 32 * g) : 0;
-            const int nb_n = small_n ? min(32, a.N - 32 * g) : 0;
-            int cr = 0, cn = 0;
-            for (int b = 0; b < nb_r; ++b) {
-                const uint32_t m = __ballot_sync(0xffffffffu, (rm >> (32 * g + b)) & 1ull);
-                if (lane == b) cr = __popc(m);
+            if (small_r && 32 * g < a.R) {
+                const int cr = bit_column_count((uint32_t)(rm >> (32 * g)), lane);
+                if (cr) atomicAdd(&col_agg[a.E + 32 * g + lane], cr);
             }
-            for (int b = 0; b < nb_n; ++b) {
-                const uint32_t m = __ballot_sync(0xffffffffu, (nm >> (32 * g + b)) & 1ull);
-                if (lane == b) cn = __popc(m);
+            if (small_n && 32 * g < a.N) {
+                const int cn = bit_column_count((uint32_t)(nm >> (32 * g)), lane);
+                if (cn) atomicAdd(&col_agg[a.E + a.R + 32 * g + lane], cn);
             }
-            if (cr) atomicAdd(&col_agg[a.E + 32 * g + lane], cr);
-            if (cn) atomicAdd(&col_agg[a.E + a.R + 32 * g + lane], cn);
         }
     }
     __syncthreads();
@@ -338,7 +358,19 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     if (a.in_rank) {
         uint8_t *blk = a.in_rank + (int64_t)t0 * a.R;
         const int nbytes = ntok * a.R;
-        if (small_r && (a.R & 3) == 0 && (reinterpret_cast<uintptr_t>(blk) & 3) == 0) {
+        if (small_r && (a.R & 15) == 0 && (reinterpret_cast<uintptr_t>(a.in_rank) & 15) == 0) {
+            // one token per thread: its row of R bytes as 16-byte vectors, byte r = bit r
+            // of the token's rank mask (rows are 16-byte aligned as R % 16 == 0)
+            for (int tl = tid; tl < ntok; tl += kThreads) {
+                const unsigned long long m = tok_rmask[tl];
+                int4 *dst = reinterpret_cast<int4 *>(blk + (int64_t)tl * a.R);
+                for (int v = 0; v < (a.R >> 4); ++v) {
+                    const uint32_t bits = (uint32_t)(m >> (16 * v));
+                    dst[v] = make_int4(spread4(bits), spread4(bits >> 4), spread4(bits >> 8),
+                                       spread4(bits >> 12));
+                }
+            }
+        } else if (small_r && (a.R & 3) == 0 && (reinterpret_cast<uintptr_t>(blk) & 3) == 0) {
             // each word holds 4 ranks of one token: spread 4 mask bits into 4 bytes
             const int wpr = a.R >> 2;  // words per row
             uint32_t *words = reinterpret_cast<uint32_t *>(blk);
@@ -724,8 +756,6 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     a.start_out = start_out;
     a.total_out = total_out;
     a.alignment = alignment;
-    a.id_bits = 0;
-    while ((1 << a.id_bits) < E) ++a.id_bits;
     auto log2_exact = [](int v) {
         int b = 0;
         while ((1 << b) < v) ++b;
