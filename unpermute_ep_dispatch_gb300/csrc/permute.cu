@@ -164,11 +164,11 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a) {
 }
 
 // ----------------------------------------------------------------------------- bulk-copy variant
-// One block per SM, each over a contiguous run of tokens. For a batch of tokens
-// all threads first resolve the slots; then thread 0 streams the rows through a
-// ring of shared-memory stages -- one bulk load of each row from HBM and, as soon
-// as it lands, k bulk stores of it to its slots -- while the other warps copy the
-// small fp8 scale rows. The row copies run on the TMA engine instead of the
+// Blocks over contiguous runs of tokens. For a batch of tokens all threads first
+// resolve the slots; then warp 0 streams the rows through a ring of shared-memory
+// stages -- one bulk load of each row from HBM and, as soon as it lands, k bulk
+// stores of it to its slots, issued by k lanes at once -- while the other warps copy
+// the small fp8 scale rows. The row copies run on the TMA engine instead of the
 // load/store units, whose store queue limits the register variant above.
 constexpr int kTmaThreads = 256;
 constexpr size_t kTmaStageBudget = 64 * 1024;  // shared memory for row stages (a few blocks per SM)
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     int *s_list = reinterpret_cast<int *>(tsm + L.list_off);   // tokens of the batch with a slot
     uint64_t *bars = reinterpret_cast<uint64_t *>(tsm + L.bars_off);
     int32_t *s_seg = reinterpret_cast<int32_t *>(tsm + L.seg_off);  // [nseg] offsets, [nseg] counts
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = tma_batch_tokens(a.k);
     const int S = L.stages;
     const uint32_t bytes = (uint32_t)a.row_bytes;
@@ -226,10 +226,10 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
         mbar_init_fence();
     }
     pdl_wait();  // offsets and pair ranks come from the previous kernels
-    int pre = 0;  // rows of the first batch loaded ahead (thread 0)
+    // rows of the first batch loaded ahead (by thread 0)
+    const int pre = whole ? min(S - 1, min(B, t_end - t_begin)) : 0;
     if (tid == 0) {
         if (whole) {
-            pre = min(S - 1, min(B, t_end - t_begin));
             for (int i = 0; i < pre; ++i) {
                 mbar_expect_tx(&bars[i], bytes);
                 bulk_load(stage + i * L.row_stride, a.x + (int64_t)(t_begin + i) * a.row_bytes,
@@ -287,7 +287,10 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
             }
             __syncthreads();
         }
-        if (tid == 0) {
+        if (warp == 0) {
+            // Warp 0 streams the rows: lane 0 issues the loads, every lane waits on the
+            // landed stage's barrier, and lanes j < k issue the k stores of the row at
+            // once (each lane in its own bulk group).
             const int n = whole ? nb : s_n;
             int issued = b0 == t_begin ? pre : 0, landed = 0;
             auto token = [&](int i) { return whole ? i : s_list[i]; };
@@ -297,27 +300,35 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
                 bulk_load(stage + st * L.row_stride, a.x + (int64_t)(b0 + token(i)) * a.row_bytes,
                           bytes, &bars[st]);
             };
-            for (; issued < min(n, S - 1); ++issued) load(issued);
+            const int first = min(n, S - 1);
+            if (lane == 0)
+                for (int i = issued; i < first; ++i) load(i);
+            issued = max(issued, first);
             for (; landed < n; ++landed) {
                 const uint32_t r = seq + landed, st = r % S;
-                if (!mbar_wait_bounded(&bars[st], (r / S) & 1u, kTmaWaitLimit)) {
-                    report(a.status, EPD_ERR_TIMEOUT);
-                    s_failed = 1;
+                const bool ok = mbar_wait_bounded(&bars[st], (r / S) & 1u, kTmaWaitLimit);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) {
+                        report(a.status, EPD_ERR_TIMEOUT);
+                        s_failed = 1;
+                    }
                     break;
                 }
                 fence_proxy_async_smem();
                 const int *sl = s_slot + token(landed) * a.k;
-                for (int j = 0; j < a.k; ++j)
+                for (int j = lane; j < a.k; j += 32)
                     if (sl[j] >= 0)
                         bulk_store(a.out + (int64_t)sl[j] * a.row_bytes, stage + st * L.row_stride,
                                    bytes);
                 bulk_commit();
                 if (issued < n) {
-                    bulk_wait_read<1>();  // the stage of row r - 1 is free again
-                    load(issued++);
+                    bulk_wait_read<1>();  // this lane's stores of row r - 1 have left its stage
+                    __syncwarp();         // and every other lane's: the stage is free again
+                    if (lane == 0) load(issued);
+                    ++issued;
                 }
             }
-            if (s_failed) {  // let every load still in flight land before the block exits
+            if (s_failed && lane == 0) {  // let every load still in flight land before the block exits
                 for (int i = landed; i < issued; ++i) {
                     const uint32_t r = seq + i;
                     mbar_wait_bounded(&bars[r % S], (r / S) & 1u, kTmaWaitLimit);
@@ -347,7 +358,7 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     if (!a.defer_scales)
         fill_m_indices(a, seg_start, seg_count, base, (int64_t)blockIdx.x * kTmaThreads + tid,
                        (int64_t)gridDim.x * kTmaThreads);
-    if (tid == 0) bulk_wait_all();
+    if (warp == 0) bulk_wait_all();
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
