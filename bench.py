@@ -797,7 +797,7 @@ def run_epd(args, rank, world, local):
     M, A = path.M, path.A
     torch.cuda.synchronize(dev)
     peak, peak_src = load_peaks()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clock_period_ms * 1e-3)
     clocks.start()
 
     for _ in range(args.warmup):
@@ -1061,7 +1061,7 @@ def run_decode(args, rank, world, local):
     G = max(1, int(args.steps_per_graph))  # consecutive steps (input sets) per graph
     if args.steps % G:
         raise SystemExit(f"--steps {args.steps} is not a multiple of --steps-per-graph {G}")
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clock_period_ms * 1e-3)
     clocks.start()
     barrier(world, dev)
     lat, tot_ms, n_steps, path_bytes, info = decode_latency(
@@ -1200,6 +1200,8 @@ def main(argv=None):
                     help="decode: fixed-rectangle layout with the fused bf16->fp8 cast")
     ap.add_argument("--decode-pool", type=int, default=16,
                     help="distinct input sets cycled by the decode workload")
+    ap.add_argument("--clock-period-ms", type=float, default=1.0,
+                    help="NVML clock sampling period (a child process samples)")
     ap.add_argument("--record-traffic", default=None, metavar="CSV",
                     help="write profiles/ncu_traffic.json from an ncu CSV and exit")
     ap.add_argument("--traffic-workload", default="dsv3_fp8")

@@ -358,7 +358,9 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
     if (!a.defer_scales)
         fill_m_indices(a, seg_start, seg_count, base, (int64_t)blockIdx.x * kTmaThreads + tid,
                        (int64_t)gridDim.x * kTmaThreads);
-    if (warp == 0) bulk_wait_all();
+    // the stages must stay valid until the last stores have read them; their writes
+    // complete on their own (the grid's completion covers them)
+    if (warp == 0) bulk_wait_read<0>();
     // the next kernel may be scheduled now: triggering only after the row copies keeps
     // its blocks from holding SM resources while this kernel streams
     pdl_trigger();
@@ -463,9 +465,16 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
             }
         }
         if (L.total <= opted.load(std::memory_order_acquire)) {
-            // three blocks' worth of token runs per SM (measured best on GB300)
-            const int64_t full = 3 * (int64_t)sm_count();
-            const int grid = (int)(T < full ? (T < 1 ? 1 : T) : full);
+            // Short token runs, about four tokens per block, between two and sixteen blocks
+            // per SM (two resident): the hardware hands the next run to whichever block slot
+            // frees first, which balances the streams across SMs. Measured on GB300 over
+            // 2..16 blocks per SM: dsv3_fp8 and skew_bf16 want 12-16 per SM, prefill_bf16
+            // about 7; fewer, longer runs leave SMs idle in the last wave.
+            const int64_t sms = sm_count();
+            const int64_t want = (T + 3) / 4;
+            int64_t g = want < 2 * sms ? 2 * sms : (want > 16 * sms ? 16 * sms : want);
+            if (g > T) g = T;
+            const int grid = (int)(g < 1 ? 1 : g);
             return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
         }
     }
