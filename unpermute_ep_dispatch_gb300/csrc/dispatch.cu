@@ -145,18 +145,20 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     if (warp == 0) {
         const int per = (a.E + 31) / 32;
         const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
+        const int A = a.alignment;
+        auto padded = [A](int c) { return A == 1 ? c : (c + A - 1) / A * A; };
         int run = 0, pairs = 0;
         for (int e = e0; e < e1; ++e) {
             const int c = s_cnt[e];
             pairs += c;
-            run += (c + a.alignment - 1) / a.alignment * a.alignment;
+            run += padded(c);
         }
         const int incl = warp_incl_scan(run, lane);
         pairs = warp_sum(pairs);
         int pos = incl - run;
         for (int e = e0; e < e1; ++e) {
             s_start[e] = pos;
-            pos += (s_cnt[e] + a.alignment - 1) / a.alignment * a.alignment;
+            pos += padded(s_cnt[e]);
         }
         if (lane == 31) {
             s_total = incl;
@@ -308,9 +310,10 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
             a.hdr->num_topk = a.k;
         }
     }
-    // the bulk stores read shared memory until they complete; loads that outlived a
-    // wait that gave up land before the block's shared memory is released
-    if (issued) bulk_wait_all();
+    // the bulk stores read shared memory until they have read it (their writes then
+    // complete on their own: the grid's completion covers them); loads that outlived
+    // a wait that gave up land before the block's shared memory is released
+    if (issued) bulk_wait_read<0>();
     if (tid == 0 && copy && !s_rows_ok) mbar_wait_bounded(&s_bar, 0u, kWaitLimit);
     pdl_trigger();
 }

@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
             if (a.per_expert) a.per_expert[e] = tot;
             a.ws_counts[e] = tot;
             part += tot;
-            run += (tot + a.alignment - 1) / a.alignment * a.alignment;
+            run += a.alignment == 1 ? tot : (tot + a.alignment - 1) / a.alignment * a.alignment;
         }
         for (int c = a.E + tid; c < a.cols; c += kThreads) {
             const int tot = col_excl[c] + col_agg[c];
@@ -552,7 +552,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
             int pos = s_red[warp] + incl - run;
             for (int e = e0; e < e1; ++e) {
                 a.start_out[e] = pos;
-                pos += (col_excl[e] + col_agg[e] + a.alignment - 1) / a.alignment * a.alignment;
+                const int tot = col_excl[e] + col_agg[e];
+                pos += a.alignment == 1 ? tot : (tot + a.alignment - 1) / a.alignment * a.alignment;
             }
         }
     }
