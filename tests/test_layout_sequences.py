@@ -222,3 +222,34 @@ def test_leftover_state_words_are_ignored(plant):
     assert int(ws[8:16].view(torch.int64).item()) == epoch + 1   # the tile form ran
     _check_layout("offsets", small, os_, f"after planting {plant}")
     _check_ranks(small, ws, st, os_.start, f"after planting {plant}")
+
+
+# ----------------------------------------------------------------------------- the two layout forms
+# Batches of up to 16 x 8192 (token, pick) pairs (E <= 1024, <= 2048 tokens per block)
+# run the cluster form; larger ones the tile form. Each case below sits on an edge of
+# that choice or of the cluster form itself, and the whole path is compared with the
+# oracle (counts, masks, offsets, slots, rows, combine).
+FORM_EDGES = [
+    # T, k, E, R, N
+    (129, 64, 16, 8, 2),        # 16 blocks; the last one holds no token
+    (3000, 8, 640, 64, 8),      # 16 warps per block (E > 512), four chunks per warp
+    (2048, 8, 256, 128, 2),     # R > 64: distinct ranks counted by comparing picks
+    (1500, 8, 512, 256, 128),   # R and N > 64
+    (1000, 6, 90, 9, 3),        # E/R and R/N not powers of two (table look-ups)
+    (32768, 1, 256, 32, 4),     # k = 1 at the 2048-token block limit
+    (32769, 1, 256, 32, 4),     # one token over it: the tile form
+    (16385, 8, 256, 32, 4),     # one token over the cluster's pairs: the tile form
+    (1025, 1, 16, 8, 2),        # just over one tile: a cluster of two
+]
+
+
+@pytest.mark.parametrize("T,k,E,R,N", FORM_EDGES)
+@pytest.mark.parametrize("fused", [True, False])
+def test_layout_form_edges(T, k, E, R, N, fused):
+    from epd_paths import GpuPath, compare, oracle_path
+    case = workloads.make_random_case(T=T, H=16, k=k, E=E, R=R, N=N, dtype="bf16",
+                                      seed=T + 31 * k + E, routing="repeats", p_invalid=0.1,
+                                      experts="random")
+    g = GpuPath(case, fused=fused)
+    g.step()
+    compare(g.results(), oracle_path(case))
