@@ -6,26 +6,31 @@
 // is_token_in_rank. The pages skip the kernel body; this one is designed for
 // sm_103a from the definition.
 //
-// One block per token tile (tile order from an atomic ticket, so a block only
-// ever waits on blocks that are already running). Inside a tile:
+// The batch is cut into token tiles, one per block: the blocks of one
+// thread-block cluster for batches up to 16 x 8192 pairs (they exchange their
+// counts through distributed shared memory), else one block per 1024-pair tile
+// in ticket order (a block only ever waits on blocks already running). Inside a
+// tile:
 //   * each warp walks a contiguous run of the tile's (token, pick) pairs in
-//     row-major order; lanes holding the same expert find each other with one
-//     ballot per bit of the expert id, and the lowest of them adds the group's
-//     size to the warp's private shared-memory histogram (warp-aggregated, no
-//     atomics); the picks are parked in shared memory for the token masks;
+//     row-major order, 32 at a time; lanes holding the same expert find each other
+//     through a per-warp shared-memory word per expert (each sets its lane bit,
+//     then reads the word), and the lowest of them adds the group's size to the
+//     warp's private histogram; the picks are parked in shared memory for the
+//     token masks;
 //   * an exclusive scan across the warps' histograms (one thread per expert)
 //     gives each pair its rank among the tile's pairs of the same expert, in
 //     (t, j) order; beside it, other warps build each token's rank and node bit
-//     masks and count the tile's tokens per rank and per node with ballots;
-//   * the tile's counts (experts, ranks, nodes) are published and the prefix
-//     over earlier tiles is read with a single-pass decoupled look-back: a
-//     warp polls the states of up to 32 earlier tiles at once and stops at the
-//     nearest one that has published its inclusive prefix;
+//     masks and count the tile's tokens per rank and per node;
+//   * the tile's counts (experts, ranks, nodes) reach the later tiles: in the
+//     cluster, by stores into their shared memory and one cluster barrier; else
+//     they are published and read with a single-pass decoupled look-back (a warp
+//     polls the states of up to 32 earlier tiles at once and stops at the
+//     nearest one that has published its inclusive prefix);
 //   * prefix + warp base + rank inside the warp = the pair's rank inside its
 //     expert over the whole batch, stored in the workspace for ep_permute;
 //   * the tile that holds the last ticket writes the totals (and, for
 //     ep_dispatch_layout_offsets, the expert offsets).
-// A call with a single tile takes no ticket and publishes nothing. Every value
+// A tile-form call with a single tile takes no ticket and publishes nothing. Every value
 // is an integer sum, so the outputs are the same whichever order the blocks run
 // in. Waits are bounded: a wait that runs out sets EPD_ERR_TIMEOUT and the
 // block carries on.
@@ -46,7 +51,6 @@ constexpr uint64_t kStateMark = 1ull << 63;
 constexpr uint32_t kStateAgg = 1;   // tile published its own counts
 constexpr uint32_t kStateIncl = 2;  // tile published counts of itself and all earlier tiles
 constexpr uint32_t kDefaultSpinLimit = 1u << 19;  // polls with back-off: about a second
-static_assert(EPD_MAX_EXPERTS <= 4096, "expert ids fit the 12 bits the narrowest block ranks");
 
 struct LayoutArgs {
     const int64_t *topk;
@@ -83,7 +87,7 @@ __device__ __forceinline__ int warp_sum(int v) {
 // Byte offsets of the layout kernel's shared-memory regions; every region that is
 // read or written with 16-byte vectors starts on a 16-byte boundary.
 struct LayoutSmem {
-    size_t rmask, nmask, hist, agg, excl, rank_of, node_of, pick, stage, total;
+    size_t rmask, nmask, hist, lanes, agg, excl, rank_of, node_of, pick, stage, total;
 };
 
 __host__ __device__ inline LayoutSmem layout_smem(int E, int W, int cols_pad, int tile_tokens,
@@ -92,7 +96,8 @@ __host__ __device__ inline LayoutSmem layout_smem(int E, int W, int cols_pad, in
     m.rmask = 0;
     m.nmask = m.rmask + (size_t)tile_tokens * 8;
     m.hist = m.nmask + (size_t)tile_tokens * 8;
-    m.agg = align_up(m.hist + (size_t)W * (E + 1) * 4, 16);
+    m.lanes = align_up(m.hist + (size_t)W * (E + 1) * 4, 16);
+    m.agg = align_up(m.lanes + (W >= 16 ? (size_t)W * E * 4 : 0), 16);
     m.excl = m.agg + (size_t)cols_pad * 4;
     m.rank_of = m.excl + (size_t)cols_pad * 4;
     m.node_of = m.rank_of + (size_t)E * 4;
@@ -125,8 +130,9 @@ __device__ __forceinline__ int spread4(uint32_t b) { return (int)(((b & 0xFu) * 
 template <int W, int kChunks, bool kCluster>
 __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
-    // bits of the largest expert id this block width serves (layout_warps)
-    constexpr int kIdBits = W >= 32 ? 9 : W >= 16 ? 10 : W >= 8 ? 11 : 12;
+    // lane-mask words per warp and expert for E <= 1024 (16 or 32 warps); wider
+    // expert sets keep their shared memory for the histograms and use ballots
+    constexpr bool kLaneWords = W >= 16;
     extern __shared__ int4 smem_raw[];
     char *sm = reinterpret_cast<char *>(smem_raw);
     const LayoutSmem L = layout_smem(a.E, W, a.cols_pad, a.tile_tokens,
@@ -137,6 +143,9 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // per-expert scan across warps (stride of one row) hits 32 different banks
     const int hws = a.E + 1;
     int *hw = reinterpret_cast<int *>(sm + L.hist);
+    // [W][E] per warp and expert: the lanes of the warp's current chunk holding that
+    // expert (a bit mask), zero between chunks
+    uint32_t *lanes_of = reinterpret_cast<uint32_t *>(sm + L.lanes);
     int *col_agg = reinterpret_cast<int *>(sm + L.agg);    // [cols_pad] this tile's counts
     int *col_excl = reinterpret_cast<int *>(sm + L.excl);  // [cols_pad] counts of earlier tiles
     int *rank_of = reinterpret_cast<int *>(sm + L.rank_of);  // [E] simulated rank of each expert
@@ -155,6 +164,10 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         int4 *hw4 = reinterpret_cast<int4 *>(hw);
         for (int i = tid; i < n4; i += kThreads) hw4[i] = make_int4(0, 0, 0, 0);
         for (int i = 4 * n4 + tid; i < W * hws; i += kThreads) hw[i] = 0;
+        const int m4 = kLaneWords ? (W * a.E) >> 2 : 0;  // the lane masks, likewise
+        int4 *lm4 = reinterpret_cast<int4 *>(lanes_of);
+        for (int i = tid; i < m4; i += kThreads) lm4[i] = make_int4(0, 0, 0, 0);
+        for (int i = 4 * m4 + tid; kLaneWords && i < W * a.E; i += kThreads) lanes_of[i] = 0u;
     }
     for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
@@ -192,9 +205,9 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // scan across warps relies on). A full tile has kChunks chunks per warp; a
     // partial one spreads its pairs over all warps, and chunks past its last pair
     // are skipped. All of a lane's picks are loaded at once, then each chunk is
-    // ranked: lanes holding the same expert find each other with one ballot per
-    // bit of the expert id, and the lowest of them adds the group's size to the
-    // warp's private histogram.
+    // ranked: lanes holding the same expert find each other through the expert's
+    // lane-mask word, and the lowest of them adds the group's size to the warp's
+    // private histogram.
     int pe[kChunks], pr[kChunks];
     const int cpw = max(1, min(kChunks, (npairs + kThreads - 1) / kThreads));
     const int p_base = warp * 32 * cpw + lane;
@@ -214,26 +227,39 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         if (c < live && p < npairs) s_pick[p] = (int16_t)pe[c];
     }
     int *my_hist = hw + warp * hws;
+    uint32_t *my_lanes = lanes_of + warp * a.E;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         pr[c] = 0;
         if (c >= live) continue;
         const int e = pe[c];
-        uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
-        // one ballot per bit of the largest id a block of this width serves (bits above
-        // the highest bit of E - 1 are 0 for every valid lane: they change nothing)
+        // the lanes holding the same expert: every lane sets its bit in the expert's
+        // word, then reads the word back (a shared-memory atomic OR and a load cost a
+        // fraction of the one-ballot-per-id-bit search they replace); every lane reads
+        // the group's count before the group's lowest lane adds to it and clears the
+        // word for the next chunk; the warp stays converged (whole-warp syncs only)
+        uint32_t peers;
+        if constexpr (kLaneWords) {
+            if (e >= 0) atomicOr(&my_lanes[e], 1u << lane);
+            __syncwarp();
+            peers = e >= 0 ? my_lanes[e] : 0u;
+        } else {
+            // E > 1024: one ballot per id bit instead (no lane words: shared memory)
+            peers = __ballot_sync(0xffffffffu, e >= 0);
 #pragma unroll
-        for (int b = 0; b < kIdBits; ++b) {
-            const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
-            peers &= ((e >> b) & 1) ? set : ~set;
+            for (int b = 0; b < 12; ++b) {  // ids below 4096; higher bits are 0 for valid lanes
+                const uint32_t set = __ballot_sync(0xffffffffu, (e >> b) & 1);
+                peers &= ((e >> b) & 1) ? set : ~set;
+            }
         }
-        // every lane reads its group's count before the group's lowest lane adds to it;
-        // the warp stays converged (whole-warp syncs only)
         const int before = __popc(peers & lanemask_lt());
         const int base = e >= 0 ? my_hist[e] : 0;
         pr[c] = base + before;
         __syncwarp();
-        if (e >= 0 && before == 0) my_hist[e] = base + __popc(peers);
+        if (e >= 0 && before == 0) {
+            my_hist[e] = base + __popc(peers);
+            if constexpr (kLaneWords) my_lanes[e] = 0u;
+        }
         __syncwarp();
     }
 
