@@ -21,9 +21,9 @@
 //     kernel and the cross-block hand-off -- and so knows every offset;
 //   * writes its slots, bulk-stores each row to its k slots, writes its slice of
 //     m_indices and its tokens' is_token_in_rank rows;
-//   * counts the batch's tokens for its share of the ranks and nodes (block b:
-//     columns b, b + grid, ...).
-// Block 0 also writes the per-expert counts, offsets and total, and leaves the
+//   * counts the batch's tokens per rank and per node from each token's bit masks
+//     (a bit-matrix transpose of each warp's masks; every block counts the batch).
+// Block 0 also writes all the counts, the offsets and the total, and leaves the
 // workspace as the layout kernel would (header, counts, pair ranks), so a later
 // ep_permute on the same workspace sees the same state. Larger batches run the
 // layout and permute kernels.
@@ -41,7 +41,6 @@ constexpr int kSmallTokens = 1024;    // T of the one-kernel form (block 0 count
 constexpr int kSmallBlockPairs = 128; // pairs of one block's tokens
 constexpr size_t kSmallRowBytes = 96 * 1024;  // shared memory for one block's rows
 constexpr uint32_t kWaitLimit = 1u << 24;      // mbarrier polls before the row wait gives up
-constexpr int kSmallCols = 4;                  // rank / node columns one block tallies at most
 
 struct SmallArgs {
     const uint8_t *x;
@@ -87,10 +86,10 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     __shared__ int s_cnt[kSmallExperts];    // pairs per expert
     __shared__ int s_start[kSmallExperts];  // (aligned) offsets
     __shared__ uint8_t s_rank_of[kSmallExperts], s_node_of[64];
-    __shared__ int s_rank[kSmallBlockPairs], s_slot[kSmallBlockPairs];
+    __shared__ int s_rank[kSmallBlockPairs];
     __shared__ int s_total, s_pairs;
     __shared__ bool s_rows_ok;
-    __shared__ int s_col[kSmallCols];  // this block's tallies of tokens per rank / node
+    __shared__ int s_col[128];  // the batch's tokens per rank [0, R) and per node [64, 64 + N)
     __shared__ __align__(8) uint64_t s_bar;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P_all = a.T * a.k;
@@ -105,7 +104,7 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     }
     for (int r = tid; r < a.R; r += kThreads) s_node_of[r] = (uint8_t)(r / a.rpn);
     for (int q = tid; q < kSmallBlockPairs; q += kThreads) s_rank[q] = 0;
-    if (tid < kSmallCols) s_col[tid] = 0;
+    for (int i = tid; i < 128; i += kThreads) s_col[i] = 0;
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         mbar_init_fence();
@@ -125,10 +124,21 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     if (tid >= 32 && tid < 96 && tid - 32 < nsc)
         sc = a.x_scale[(int64_t)t_begin * a.scale_cols + tid - 32];
 
-    // the batch's picks, counted per expert as they arrive; ids outside [-1, E) are
-    // reported (by block 0) and skipped
-    for (int p = tid; p < P_all; p += kThreads) {
-        const int64_t v = a.topk[p];
+    // the batch's picks: all of a thread's loads are issued first (one round trip, not
+    // one per pick), then parked in shared memory and counted per expert; ids outside
+    // [-1, E) are reported (by block 0) and skipped
+    constexpr int kPicksPerThread = kSmallPairs / kThreads;
+    int64_t pv[kPicksPerThread];
+#pragma unroll
+    for (int i = 0; i < kPicksPerThread; ++i) {
+        const int p = tid + i * kThreads;
+        pv[i] = p < P_all ? __ldg(a.topk + p) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kPicksPerThread; ++i) {
+        const int p = tid + i * kThreads;
+        if (p >= P_all) break;
+        const int64_t v = pv[i];
         const bool ok = v >= 0 && v < a.E;
         if ((v < -1 || v >= a.E) && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_EXPERT);
         s_e[p] = ok ? (int16_t)v : (int16_t)-1;
@@ -183,30 +193,38 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     }
     __syncthreads();
 
-    // slots of this block's pairs
-    for (int q = tid; q < q_end; q += kThreads) {
-        const int p = p0 + q;
-        const int e = s_e[p];
-        int s = -1;
-        if (e >= 0) {
-            const int64_t sl = (int64_t)s_start[e] + s_rank[q];
-            if (sl < a.capacity) s = (int)sl;
-            else report(a.status, EPD_ERR_CAPACITY);
-        }
-        s_slot[q] = s;
-        a.output_index[p] = s;
-        a.pair_rank[p] = e >= 0 ? s_rank[q] : -1;
-    }
-    __syncthreads();
+    // the slot of this block's pair q (-1 for no pick, or past the buffer); every warp
+    // that needs slots computes them itself, so no barrier separates them from the
+    // copies
+    auto slot_of = [&](int q) {
+        const int e = s_e[p0 + q];
+        if (e < 0) return -1;
+        const int64_t sl = (int64_t)s_start[e] + s_rank[q];
+        return sl < a.capacity ? (int)sl : -1;
+    };
 
-    // warp 0 (thread 0) moves the rows: once they have landed, k bulk stores each
-    // from shared memory. Meanwhile warps 1 and 2 copy the scale words (the ones
-    // loaded at the start), warp 3 writes this block's slice of m_indices, warp 4
-    // its tokens' is_token_in_rank rows, and warps 5.. tally the batch's tokens for
-    // this block's share of the rank and node columns.
-    const int cols = a.R + (a.per_node ? a.N : 0);
+    // warp 0 writes the block's slots (output_index and the workspace's pair ranks)
+    // and moves the rows: once they have landed, lane i issues the bulk stores of
+    // pairs i, i + 32, ... from shared memory. Meanwhile warps 1 and 2 copy the scale
+    // words (the ones loaded at the start), warp 3 writes this block's slice of
+    // m_indices, and warps 4..7 build the batch's token masks, write this block's
+    // is_token_in_rank rows and count the batch's tokens per rank and per node.
     bool issued = false;  // this lane of warp 0 has bulk stores in flight
     if (warp == 0) {
+        constexpr int kPerLane = kSmallBlockPairs / 32;
+        int sl[kPerLane];
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int q = lane + 32 * i;
+            sl[i] = -1;
+            if (q < q_end) {
+                const int e = s_e[p0 + q];
+                sl[i] = slot_of(q);
+                if (e >= 0 && sl[i] < 0) report(a.status, EPD_ERR_CAPACITY);
+                a.output_index[p0 + q] = sl[i];
+                a.pair_rank[p0 + q] = e >= 0 ? s_rank[q] : -1;
+            }
+        }
         bool landed = true;
         if (copy) {
             if (lane == 0) landed = mbar_wait_bounded(&s_bar, 0u, kWaitLimit);
@@ -216,12 +234,12 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
                 if (!landed) report(a.status, EPD_ERR_TIMEOUT);
             }
             if (landed) {
-                // lane i issues the stores of (token, pick) pairs i, i + 32, ...
                 fence_proxy_async_smem();
-                for (int q = lane; q < q_end; q += 32) {
-                    const int s = s_slot[q];
-                    if (s < 0) continue;
-                    bulk_store(a.out + (int64_t)s * a.row_bytes, s_rows + (q / a.k) * stride,
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i) {
+                    const int q = lane + 32 * i;
+                    if (q >= q_end || sl[i] < 0) continue;
+                    bulk_store(a.out + (int64_t)sl[i] * a.row_bytes, s_rows + (q / a.k) * stride,
                                (uint32_t)a.row_bytes);
                     issued = true;
                 }
@@ -234,7 +252,7 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
             const int tl = i / a.scale_cols, c = i - tl * a.scale_cols;
             const uint32_t v = i == wt ? sc : a.x_scale[(int64_t)t_begin * a.scale_cols + i];
             for (int j = 0; j < a.k; ++j) {
-                const int s = s_slot[tl * a.k + j];
+                const int s = slot_of(tl * a.k + j);
                 if (s >= 0) a.out_scale[(int64_t)s * a.scale_cols + c] = v;
             }
         }
@@ -254,50 +272,55 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
             const int64_t st = s_start[lo];
             a.m_indices[s] = (s >= st && s < st + s_cnt[lo]) ? lo : -1;
         }
-    } else if (warp == 4) {
-        if (a.in_rank)
-            for (int i = lane; i < nt * a.R; i += 32) {
-                const int tl = i / a.R, r = i - tl * a.R;
-                const int16_t *row = s_e + (t_begin + tl) * a.k;
-                bool hit = false;
-                for (int j = 0; j < a.k && !hit; ++j) hit = row[j] >= 0 && s_rank_of[row[j]] == r;
-                a.in_rank[(int64_t)(t_begin + tl) * a.R + r] = hit ? 1 : 0;
-            }
     } else {
-        // column cb of this block is col = blockIdx.x + cb * grid; 32 tokens per ballot
-        const int nwt = kThreads - 160;  // threads of warps 5..
-        for (int cb = 0; cb < kSmallCols; ++cb) {
-            const int col = blockIdx.x + cb * gridDim.x;
-            if (col >= cols) break;
-            const bool is_rank = col < a.R;
-            const int target = is_rank ? col : col - a.R;
-            for (int t0 = (warp - 5) * 32; t0 < a.T; t0 += nwt) {
-                const int t = t0 + lane;
-                bool hit = false;
-                if (t < a.T) {
-                    const int16_t *row = s_e + t * a.k;
-                    for (int j = 0; j < a.k && !hit; ++j) {
-                        const int e = row[j];
-                        if (e < 0) continue;
-                        const int r = s_rank_of[e];
-                        hit = is_rank ? r == target : s_node_of[r] == target;
+        // warps 4..7, one lane per token of the batch: the token's rank and node bit
+        // masks from its picks (R, N <= 64 in this form); its is_token_in_rank row when
+        // it is one of this block's tokens; and the batch's tokens per rank and per node
+        // by counting the columns of each warp's masks. Every block counts the whole
+        // batch (a few hundred tokens); block 0 writes the counts.
+        const bool words = (a.R & 3) == 0 && (reinterpret_cast<uintptr_t>(a.in_rank) & 3) == 0;
+        for (int t0 = (warp - 4) * 32; t0 < a.T; t0 += 128) {
+            const int t = t0 + lane;
+            unsigned long long rm = 0, nm = 0;
+            if (t < a.T) {
+                const int16_t *row = s_e + t * a.k;
+                for (int j = 0; j < a.k; ++j) {
+                    const int e = row[j];
+                    if (e < 0) continue;
+                    const int r = s_rank_of[e];
+                    rm |= 1ull << r;
+                    nm |= 1ull << s_node_of[r];
+                }
+                if (a.in_rank && t >= t_begin && t < t_end) {
+                    uint8_t *dst = a.in_rank + (int64_t)t * a.R;
+                    if (words) {
+                        for (int w4 = 0; w4 < (a.R >> 2); ++w4)
+                            reinterpret_cast<int *>(dst)[w4] = spread4((uint32_t)(rm >> (4 * w4)));
+                    } else {
+                        for (int r = 0; r < a.R; ++r) dst[r] = (uint8_t)((rm >> r) & 1ull);
                     }
                 }
-                const uint32_t m = __ballot_sync(0xffffffffu, hit);
-                if (lane == 0 && m) atomicAdd(&s_col[cb], __popc(m));
+            }
+            for (int g = 0; g < 2; ++g) {
+                if (32 * g < a.R) {
+                    const int c = bit_column_count((uint32_t)(rm >> (32 * g)), lane);
+                    if (c) atomicAdd(&s_col[32 * g + lane], c);
+                }
+                if (a.per_node && 32 * g < a.N) {
+                    const int c = bit_column_count((uint32_t)(nm >> (32 * g)), lane);
+                    if (c) atomicAdd(&s_col[64 + 32 * g + lane], c);
+                }
             }
         }
     }
     __syncthreads();
-    for (int cb = tid; cb < kSmallCols; cb += kThreads) {
-        const int col = blockIdx.x + cb * gridDim.x;
-        if (col >= cols) continue;
-        if (col < a.R) a.per_rank[col] = s_col[cb];
-        else a.per_node[col - a.R] = s_col[cb];
-    }
 
-    // block 0: per-expert counts, offsets and total, and the workspace header and counts
+    // block 0: per-expert, per-rank and per-node counts, offsets and total, and the
+    // workspace header and counts
     if (blockIdx.x == 0) {
+        for (int c = tid; c < a.R; c += kThreads) a.per_rank[c] = s_col[c];
+        if (a.per_node)
+            for (int c = tid; c < a.N; c += kThreads) a.per_node[c] = s_col[64 + c];
         for (int e = tid; e < a.E; e += kThreads) {
             a.per_expert[e] = s_cnt[e];
             a.ws_counts[e] = s_cnt[e];
@@ -371,7 +394,7 @@ extern "C" epd_status_t ep_dispatch(const void *x, epd_dtype_t dtype, const floa
     const size_t smem = (size_t)tokens_per_block * small_row_stride(row_bytes);
     const bool small = (int64_t)T * k <= kSmallPairs && T <= kSmallTokens && E <= kSmallExperts &&
                        R <= 64 && N <= 64 && (int64_t)tokens_per_block * k <= kSmallBlockPairs &&
-                       smem <= kSmallRowBytes && (int64_t)grid * kSmallCols >= R + N;
+                       smem <= kSmallRowBytes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!small) {
         const epd_status_t st = ep_dispatch_layout_offsets(

@@ -107,26 +107,6 @@ __host__ __device__ inline LayoutSmem layout_smem(int E, int W, int cols_pad, in
     return m;
 }
 
-// Lane b gets the number of lanes of the warp whose word x has bit b set: the warp's
-// 32 x 32 bit matrix is transposed by five butterfly exchanges of half-blocks, and
-// each lane then counts the bits of its row.
-__device__ __forceinline__ int bit_column_count(uint32_t x, int lane) {
-#pragma unroll
-    for (int j = 16; j >= 1; j >>= 1) {
-        const uint32_t m = j == 16 ? 0x0000ffffu
-                         : j == 8  ? 0x00ff00ffu
-                         : j == 4  ? 0x0f0f0f0fu
-                         : j == 2  ? 0x33333333u
-                                   : 0x55555555u;
-        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
-        x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y & m) << j));
-    }
-    return __popc(x);
-}
-
-// The low four bits of b spread to the four bytes of a word (byte i = bit i).
-__device__ __forceinline__ int spread4(uint32_t b) { return (int)(((b & 0xFu) * 0x00204081u) & 0x01010101u); }
-
 template <int W, int kChunks, bool kCluster>
 __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;

@@ -234,8 +234,20 @@ __global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs 
         for (int tl = 0; tl < nt; ++tl)
             bulk_load(s_x + tl * stride, a.x + (int64_t)(t_begin + tl) * bytes, bytes, &s_bar);
     }
-    for (int p = tid; p < P_all; p += kThreads) {
-        const int64_t v = a.topk[p];
+    // the batch's picks: all of a thread's loads are issued first (one round trip),
+    // then parked in shared memory
+    constexpr int kPicksPerThread = kLLSmallPairs / kThreads;
+    int64_t pv[kPicksPerThread];
+#pragma unroll
+    for (int i = 0; i < kPicksPerThread; ++i) {
+        const int p = tid + i * kThreads;
+        pv[i] = p < P_all ? __ldg(a.topk + p) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kPicksPerThread; ++i) {
+        const int p = tid + i * kThreads;
+        if (p >= P_all) break;
+        const int64_t v = pv[i];
         const bool ok = v >= 0 && v < a.E;
         if ((v < -1 || v >= a.E) && first) report(a.status, EPD_ERR_INVALID_EXPERT);
         s_e[p] = ok ? (int16_t)v : (int16_t)-1;
