@@ -147,15 +147,37 @@ def _function_bodies(text: str):
     return out
 
 
+def _function_name(body: str) -> str:
+    head = body.split("{", 1)[0]
+    m = re.findall(r"(\w+)\s*\(", head)
+    return m[-1] if m else ""
+
+
 def device_code_hash(sources) -> str:
     """Hash of the device code a kernel is built from: the __global__ / __device__
-    functions of its source files and of the shared header. Host-side edits (launch
-    set-up, argument checks) leave it unchanged; any kernel edit changes it."""
-    h = hashlib.sha256()
-    for name in list(sources) + ["epd_common.cuh"]:
+    functions of its source files, and the shared header's device functions that
+    they call (directly or through one another). Host-side edits (launch set-up,
+    argument checks) and header functions the kernel does not use leave it
+    unchanged; any edit of the kernel or of a function it calls changes it."""
+    own = []
+    for name in sources:
         with open(os.path.join(CSRC, name)) as f:
-            for body in _function_bodies(f.read()):
-                h.update(body.encode())
+            own += _function_bodies(f.read())
+    with open(os.path.join(CSRC, "epd_common.cuh")) as f:
+        shared = [(_function_name(b), b) for b in _function_bodies(f.read())]
+    used, todo = set(), list(own)
+    while todo:
+        text = todo.pop()
+        for fn, b in shared:
+            if fn not in used and re.search(r"\b" + re.escape(fn) + r"\s*[<(]", text):
+                used.add(fn)
+                todo += [b2 for fn2, b2 in shared if fn2 == fn]
+    h = hashlib.sha256()
+    for body in own:
+        h.update(body.encode())
+    for fn, body in shared:      # file order; overloads share a name
+        if fn in used:
+            h.update(body.encode())
     return h.hexdigest()[:16]
 
 

@@ -470,8 +470,11 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
             // frees first, which balances the streams across SMs. Measured on GB300 over
             // 2..16 blocks per SM: dsv3_fp8 and skew_bf16 want 12-16 per SM, prefill_bf16
             // about 7; fewer, longer runs leave SMs idle in the last wave.
+            // A view of a few experts copies few rows: there the blocks' fixed costs
+            // dominate and three blocks per SM stay best.
             const int64_t sms = sm_count();
-            const int64_t want = (T + 3) / 4;
+            const bool wide = 4 * (int64_t)(a.e_end - a.e_begin) >= a.E;
+            const int64_t want = wide ? (T + 3) / 4 : 3 * sms;
             int64_t g = want < 2 * sms ? 2 * sms : (want > 16 * sms ? 16 * sms : want);
             if (g > T) g = T;
             const int grid = (int)(g < 1 ? 1 : g);
