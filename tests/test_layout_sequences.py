@@ -6,8 +6,8 @@ calls are issued back to back on one stream and one workspace, with different
 topk_idx and nothing in between, and each call's outputs are compared element by
 element with the oracle -- the counts, masks and offsets, and the second call's
 per-pair ranks through the permute that follows it (output_index, m_indices).
-Sizes span one-wave grids (dsv3: 64 tiles) and grids with more tiles than
-resident blocks (524 288 pairs: 512 tiles).
+Sizes span the cluster form (dsv3: 16 blocks) and the tile form with its
+ticket and look-back (524 288 pairs: 128 tiles of 4096 pairs).
 
 A second group plants leftovers in the look-back state region of a workspace
 (values an earlier call of another shape, or an earlier call, leaves there) and
@@ -169,8 +169,9 @@ def test_lowlatency_large_path_then_layout():
 
 # ----------------------------------------------------------------------------- leftovers
 def _tile_tokens(k):
-    # tokens per layout tile: 1024 (token, pick) pairs, at most 2048 tokens
-    return max(1, min(2048, 1024 // k)) if k > 0 else 2048
+    # tokens per tile of the layout's tile form at E = 256 (32-warp blocks): 4096
+    # (token, pick) pairs, at most 2048 tokens
+    return max(1, min(2048, 4096 // k)) if k > 0 else 2048
 
 
 def _state_region(T, k):

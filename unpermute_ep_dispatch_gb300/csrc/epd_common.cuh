@@ -29,7 +29,8 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 64, "header is one 64-byte block");
 
 constexpr size_t kAlign = 256;
-constexpr int kLayoutTilePairs = 1024;     // (token, pick) pairs per layout tile
+constexpr int kLayoutTilePairs = 1024;    // (token, pick) pairs per tile of 4- and 8-warp blocks
+constexpr int kLayoutWideChunks = 4;      // 32-pair chunks per warp of 16- and 32-warp blocks
 constexpr int kLayoutMaxTileTokens = 2048;
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -40,10 +41,18 @@ __host__ __device__ inline int layout_warps(int E) {
     return E <= 512 ? 32 : E <= 1024 ? 16 : E <= 2048 ? 8 : 4;
 }
 
-// Tokens per layout tile: at most kLayoutTilePairs pairs and at most 2048 tokens (one 64-bit
-// rank mask and one node mask per token stay in shared memory).
-__host__ __device__ inline int layout_tile_tokens(int k) {
-    const int t = k > 0 ? kLayoutTilePairs / k : kLayoutMaxTileTokens;
+// (token, pick) pairs per tile of the layout's tile form: four 32-pair chunks per warp of
+// a 16- or 32-warp block (E <= 1024: fewer tiles, a shorter look-back), 1024 pairs for
+// the narrow blocks of E > 1024.
+__host__ __device__ inline int layout_tile_pairs(int E) {
+    const int W = layout_warps(E);
+    return W >= 16 ? W * 32 * kLayoutWideChunks : kLayoutTilePairs;
+}
+
+// Tokens per layout tile: at most layout_tile_pairs(E) pairs and at most 2048 tokens (one
+// 64-bit rank mask and one node mask per token stay in shared memory).
+__host__ __device__ inline int layout_tile_tokens(int k, int E) {
+    const int t = k > 0 ? layout_tile_pairs(E) / k : kLayoutMaxTileTokens;
     return t < 1 ? 1 : (t < kLayoutMaxTileTokens ? t : kLayoutMaxTileTokens);
 }
 
@@ -61,7 +70,7 @@ __host__ __device__ inline size_t ws_counts_off(int T, int k) {
 
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int R, int N) {
     WsLayout w;
-    int tile = layout_tile_tokens(k);
+    int tile = layout_tile_tokens(k, E);
     w.tiles = T > 0 ? (T + tile - 1) / tile : 1;
     w.cols = E + R + N;
     w.cols_pad = (int)align_up((size_t)w.cols, 32);

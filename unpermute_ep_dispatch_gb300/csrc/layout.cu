@@ -8,7 +8,8 @@
 //
 // The batch is cut into token tiles, one per block: the blocks of one
 // thread-block cluster for batches up to 16 x 8192 pairs (they exchange their
-// counts through distributed shared memory), else one block per 1024-pair tile
+// counts through distributed shared memory), else one block per tile of
+// layout_tile_pairs(E) pairs
 // in ticket order (a block only ever waits on blocks already running). Inside a
 // tile:
 //   * each warp walks a contiguous run of the tile's (token, pick) pairs in
@@ -759,7 +760,7 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     a.agg = reinterpret_cast<int32_t *>(ws + w.agg_off);
     a.incl = reinterpret_cast<int32_t *>(ws + w.incl_off);
     a.tiles = w.tiles;
-    a.tile_tokens = layout_tile_tokens(k);
+    a.tile_tokens = layout_tile_tokens(k, E);
     a.start_out = start_out;
     a.total_out = total_out;
     a.alignment = alignment;
@@ -786,11 +787,14 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     }
     const size_t smem = layout_smem_bytes(E, w.cols_pad, a.tile_tokens,
                                           (int64_t)a.tile_tokens * k, 0);
-    switch (layout_warps(E)) {  // one 1024-pair tile per block
-        case 32: return launch_tiles<32, 1>(a, smem, stream);
-        case 16: return launch_tiles<16, 2>(a, smem, stream);
-        case 8: return launch_tiles<8, 4>(a, smem, stream);
-        default: return launch_tiles<4, 8>(a, smem, stream);
+    // a batch of one warp chunk per warp (a decode step) takes the one-chunk build
+    if (a.tiles == 1 && (int64_t)T * k <= 1024 && layout_warps(E) == 32)
+        return launch_tiles<32, 1>(a, smem, stream);
+    switch (layout_warps(E)) {  // one tile of layout_tile_pairs(E) pairs per block
+        case 32: return launch_tiles<32, kLayoutWideChunks>(a, smem, stream);
+        case 16: return launch_tiles<16, kLayoutWideChunks>(a, smem, stream);
+        case 8: return launch_tiles<8, kLayoutTilePairs / 256>(a, smem, stream);
+        default: return launch_tiles<4, kLayoutTilePairs / 128>(a, smem, stream);
     }
 }
 
