@@ -104,8 +104,9 @@ EPD_API int epd_last_cuda_error(void);
 /*
  * Workspace size in bytes for one layout -> permute chain over T tokens, k
  * picks, E experts, R ranks and N nodes. The workspace holds the per-pair rank
- * inside its expert (T*k int32) and the per-tile state of the layout's
- * single-pass look-back. Returns 0 for invalid sizes. Host-only arithmetic.
+ * inside its expert (T*k int32), the per-expert counts and, for batches beyond
+ * one thread-block cluster, the per-tile state of the layout's single-pass
+ * look-back. Returns 0 for invalid sizes. Host-only arithmetic.
  */
 EPD_API size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                            int num_rdma_ranks);
@@ -133,10 +134,13 @@ EPD_API epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_strea
  *                                   (torch.bool layout); may be NULL.
  * and, in `workspace` (epd_workspace_bytes(T, k, E, R, N) bytes), the rank of
  * every pair among the pairs of its expert in token-major (t, then j) order,
- * which ep_permute turns into slots. The ranks come from one single-pass
- * decoupled look-back scan over token tiles, so the result does not depend on
- * the order in which blocks run. Ids outside [-1, E) set
- * EPD_ERR_INVALID_EXPERT in *status and are treated as -1.
+ * which ep_permute turns into slots. The ranks come from per-tile counts and
+ * an exclusive prefix over token tiles: for up to 16 x 8192 pairs (E <= 1024)
+ * the tiles are the 2-16 blocks of one thread-block cluster, which exchange
+ * their counts through distributed shared memory; larger batches use a
+ * single-pass decoupled look-back over tiles taken in ticket order. Either way
+ * the result does not depend on the order in which blocks run. Ids outside
+ * [-1, E) set EPD_ERR_INVALID_EXPERT in *status and are treated as -1.
  */
 EPD_API epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                                 int num_experts, int num_ranks, int num_rdma_ranks,
@@ -145,8 +149,8 @@ EPD_API epd_status_t ep_dispatch_layout(const int64_t *topk_idx, int num_tokens,
                                 void *workspace, int32_t *status, epd_stream_t stream);
 
 /*
- * Steps 1 and 2 in one launch: ep_dispatch_layout, and the block that finishes
- * the look-back last also writes expert_start_loc and *total_rows exactly as
+ * Steps 1 and 2 in one launch: ep_dispatch_layout, and the block of the last
+ * token tile, once it has the totals, also writes expert_start_loc and *total_rows exactly as
  * ep_scan_offsets_aligned(tokens_per_expert, alignment) would (alignment 1 gives
  * ep_scan_offsets). Saves one launch and one kernel per pass; same arguments and
  * errors as ep_dispatch_layout otherwise.
@@ -376,7 +380,8 @@ EPD_API epd_status_t ep_unpermute(const void *expert_out, int64_t capacity_rows,
  * library routine.
  *   - Sizes whose scratch need, epd_workspace_bytes(T, k, E, R, N), exceeds
  *     EPD_NOALLOC_SCRATCH_BYTES are rejected with EPD_ERR_UNSUPPORTED before
- *     anything is launched (T*k up to about 1.5 million pairs fits at E = 256).
+ *     anything is launched (T*k up to about 1.8 million pairs fits at E = 256,
+ *     R = 32, N = 4, k = 8).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -403,7 +408,8 @@ EPD_API epd_status_t ep_dispatch_layout_noalloc(const int64_t *topk_idx, int num
 
 /*
  * Test hook for failure detection, not part of the path: runs ep_dispatch_layout
- * with the look-back wait bounded by `spin_limit` polls and with token tile
+ * in its tile form (whatever the batch size) with the look-back wait bounded by
+ * `spin_limit` polls and with token tile
  * `stalled_tile` never publishing its state, so that every later tile's wait
  * runs out. The call still completes; *status then holds EPD_ERR_TIMEOUT and
  * the counts are meaningless. The workspace stays reusable afterwards.
