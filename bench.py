@@ -566,6 +566,22 @@ def config_record(name, dev, stream, steps=20, peak=None):
     torch.cuda.synchronize(dev)
     epd.check_status(path.status, f"{name} steps")
     ms = a.elapsed_time(b) / steps
+    # the same step captured once in a CUDA graph and replayed: the device time per
+    # step without the host's launch cost (which bounds a step that fits in L2)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        path.step()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_graph = a.elapsed_time(b) / steps
+    del g
     byt = path.bytes()
     pb = byt["ep_dispatch_layout_offsets"] + byt["ep_permute"] + byt["ep_unpermute"]
     gbs = pb / (ms * 1e-3) / 1e9
@@ -574,6 +590,7 @@ def config_record(name, dev, stream, steps=20, peak=None):
            "simulated_ranks": case.R, "simulated_rdma_nodes": case.N,
            "rows": "fp8_e4m3 + f32 scale per 128 columns" if case.dtype == "fp8" else "bf16",
            "valid_pairs": path.valid_pairs(), "steps": steps, "ms_per_step": round(ms, 5),
+           "ms_per_step_graph": round(ms_graph, 5),
            "tokens_per_s": case.T / (ms * 1e-3), "path_bytes": pb, "path_gbs": round(gbs, 1),
            "frac": round(gbs / peak, 4) if peak else None,
            "launch_us_chained": {k: round(v, 2) for k, v in chained.items()},
