@@ -465,17 +465,38 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
             }
         }
         if (L.total <= opted.load(std::memory_order_acquire)) {
-            // Short token runs, about four tokens per block, between two and sixteen blocks
-            // per SM (two resident): the hardware hands the next run to whichever block slot
-            // frees first, which balances the streams across SMs. Measured on GB300 over
-            // 2..16 blocks per SM: dsv3_fp8 and skew_bf16 want 12-16 per SM, prefill_bf16
-            // about 7; fewer, longer runs leave SMs idle in the last wave.
-            // A view of a few experts copies few rows: there the blocks' fixed costs
-            // dominate and three blocks per SM stay best.
+            // Whole waves of short token runs: the grid is a whole number of resident
+            // waves (1..8), each block about six tokens; the hardware hands the next run
+            // to whichever block slot frees first, and no wave is left part-full at the
+            // end. Measured on GB300 (step / permute chained): prefill_bf16 78.8 / 38.6
+            // us at 2 waves of ~7 tokens against 81.7 / 41.5 at 3.5 waves of 4; dsv3_fp8
+            // flat from 6 to 8 waves; skew_bf16 best at 8 waves. A view of a few experts
+            // copies few rows: there the blocks' fixed costs dominate and three blocks per
+            // SM stay best.
             const int64_t sms = sm_count();
+            // resident blocks per SM at this shared-memory size (the last size asked is
+            // kept per device: (bytes << 8 | blocks))
+            static std::atomic<unsigned long long> occ_by_dev[64];
+            std::atomic<unsigned long long> occ_scratch{0};
+            std::atomic<unsigned long long> &occ =
+                (dev >= 0 && dev < 64) ? occ_by_dev[dev] : occ_scratch;
+            const unsigned long long o = occ.load(std::memory_order_acquire);
+            int per_sm = (o >> 8) == L.total ? (int)(o & 0xffu) : 0;
+            if (per_sm == 0) {
+                per_sm = blocks_per_sm(permute_tma_kernel, kTmaThreads, L.total);
+                occ.store((unsigned long long)L.total << 8 | (unsigned)(per_sm & 0xff),
+                          std::memory_order_release);
+            }
+            const int64_t slots = sms * per_sm;
             const bool wide = 4 * (int64_t)(a.e_end - a.e_begin) >= a.E;
-            const int64_t want = wide ? (T + 3) / 4 : 3 * sms;
-            int64_t g = want < 2 * sms ? 2 * sms : (want > 16 * sms ? 16 * sms : want);
+            int64_t g;
+            if (wide) {
+                int64_t waves = (T + 3 * slots) / (6 * slots);  // round(T / (6 slots))
+                waves = waves < 1 ? 1 : (waves > 8 ? 8 : waves);
+                g = waves * slots;
+            } else {
+                g = 3 * sms;
+            }
             if (g > T) g = T;
             const int grid = (int)(g < 1 ? 1 : g);
             return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
