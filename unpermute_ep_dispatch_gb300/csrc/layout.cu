@@ -9,9 +9,8 @@
 // The batch is cut into token tiles, one per block: the blocks of one
 // thread-block cluster for batches up to 16 x 8192 pairs (they exchange their
 // counts through distributed shared memory), else one block per tile of
-// layout_tile_pairs(E) pairs
-// in ticket order (a block only ever waits on blocks already running). Inside a
-// tile:
+// layout_tile_pairs(E) pairs in ticket order (a block only ever waits on blocks
+// already running). Inside a tile:
 //   * each warp walks a contiguous run of the tile's (token, pick) pairs in
 //     row-major order, 32 at a time; lanes holding the same expert find each other
 //     through a per-warp shared-memory word per expert (each sets its lane bit,
@@ -29,12 +28,12 @@
 //     nearest one that has published its inclusive prefix);
 //   * prefix + warp base + rank inside the warp = the pair's rank inside its
 //     expert over the whole batch, stored in the workspace for ep_permute;
-//   * the tile that holds the last ticket writes the totals (and, for
-//     ep_dispatch_layout_offsets, the expert offsets).
-// A tile-form call with a single tile takes no ticket and publishes nothing. Every value
-// is an integer sum, so the outputs are the same whichever order the blocks run
-// in. Waits are bounded: a wait that runs out sets EPD_ERR_TIMEOUT and the
-// block carries on.
+//   * the last tile (the last ticket, or the cluster's last block) writes the
+//     totals (and, for ep_dispatch_layout_offsets, the expert offsets).
+// A tile-form call with a single tile takes no ticket and publishes nothing.
+// Every value is an integer sum, so the outputs are the same whichever order the
+// blocks run in. Waits are bounded: a wait that runs out sets EPD_ERR_TIMEOUT and
+// the block carries on.
 #include <atomic>
 #include <cstddef>
 
