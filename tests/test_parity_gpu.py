@@ -269,6 +269,32 @@ def test_cuda_graph_replay_of_the_step():
         compare(g.results(), oracle_path(case))
 
 
+def test_cuda_graph_replay_of_the_cluster_layout_step():
+    """A dsv3-shaped step (T=2048: the layout's cluster form, 16 blocks) with the
+    layout and offsets in one launch, captured in a CUDA graph and replayed on fresh
+    routings copied into the captured buffers: every replay matches the oracle."""
+    cases = [workloads.make_case("dsv3_fp8", T=2048, seed=3000 + i) for i in range(3)]
+    g = GpuPath(cases[0], fused=True)
+    g.step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g.stream = s
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.step()
+    for case in cases:
+        g.case = case
+        g.topk.copy_(case.topk_idx)
+        g.w.copy_(case.topk_weights)
+        g.x.copy_(case.x)
+        g.xs.copy_(case.x_scale)
+        g.eo.copy_(case.expert_out)
+        torch.cuda.synchronize()
+        for _ in range(2):          # two replays in a row on one workspace
+            graph.replay()
+        compare(g.results(), oracle_path(case))
+
+
 # ----------------------------------------------------------------------------- expert alignment
 @pytest.mark.parametrize("alignment", [4, 128, 256])
 @pytest.mark.parametrize("name,T", [("tiny", None), ("dsv3_fp8", 2048), ("prefill_bf16", 1000),
