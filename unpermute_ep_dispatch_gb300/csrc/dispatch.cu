@@ -11,12 +11,12 @@
 // R and N up to 64, a block's rows within 96 KiB) is one kernel, with no hand-off
 // between blocks. Every block:
 //   * bulk-loads its own tokens' rows into shared memory and their scale words
-//     into registers as soon as it starts (they depend on nothing);
-//   * reads the whole batch's picks into shared memory and counts them per expert;
+//     into registers right after the dependency wait, before anything else;
+//   * reads the whole batch's picks into shared memory and counts them per expert,
+//     and, apart, those that come before its own first pair;
 //   * finds the ranks of its own tokens' pairs (a pair's rank inside its expert is
-//     the number of earlier pairs, in row-major order, with the same expert): all
-//     threads compare their share of the batch with up to 16 of the block's pairs
-//     at a time, then a block reduction;
+//     the number of earlier pairs, in row-major order, with the same expert): the
+//     count before the block plus the block's own earlier pairs with that expert;
 //   * scans the counts itself -- a few thousand pairs cost less than a second
 //     kernel and the cross-block hand-off -- and so knows every offset;
 //   * writes its slots, bulk-stores each row to its k slots, writes its slice of
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     extern __shared__ __align__(128) uint8_t s_rows[];  // [tokens of the block][row stride]
     __shared__ int16_t s_e[kSmallPairs];    // expert of every pair of the batch, -1 = none
     __shared__ int s_cnt[kSmallExperts];    // pairs per expert
+    __shared__ int s_before[kSmallExperts]; // pairs per expert before this block's first pair
     __shared__ int s_start[kSmallExperts];  // (aligned) offsets
     __shared__ uint8_t s_rank_of[kSmallExperts], s_node_of[64];
     __shared__ int s_rank[kSmallBlockPairs];
@@ -100,10 +101,10 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
     const bool copy = a.k > 0 && nt > 0;
     for (int e = tid; e < a.E; e += kThreads) {
         s_cnt[e] = 0;
+        s_before[e] = 0;
         s_rank_of[e] = (uint8_t)(e / a.epr);
     }
     for (int r = tid; r < a.R; r += kThreads) s_node_of[r] = (uint8_t)(r / a.rpn);
-    for (int q = tid; q < kSmallBlockPairs; q += kThreads) s_rank[q] = 0;
     for (int i = tid; i < 128; i += kThreads) s_col[i] = 0;
     if (tid == 0) {
         mbar_init(&s_bar, 1);
@@ -125,8 +126,10 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
         sc = a.x_scale[(int64_t)t_begin * a.scale_cols + tid - 32];
 
     // the batch's picks: all of a thread's loads are issued first (one round trip, not
-    // one per pick), then parked in shared memory and counted per expert; ids outside
-    // [-1, E) are reported (by block 0) and skipped
+    // one per pick), then parked in shared memory and counted per expert, and those
+    // before this block's first pair once more (the base of its pairs' ranks); ids
+    // outside [-1, E) are reported (by block 0) and skipped
+    const int p0 = t_begin * a.k, q_end = nt * a.k;
     constexpr int kPicksPerThread = kSmallPairs / kThreads;
     int64_t pv[kPicksPerThread];
 #pragma unroll
@@ -142,16 +145,18 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
         const bool ok = v >= 0 && v < a.E;
         if ((v < -1 || v >= a.E) && blockIdx.x == 0) report(a.status, EPD_ERR_INVALID_EXPERT);
         s_e[p] = ok ? (int16_t)v : (int16_t)-1;
-        if (ok) atomicAdd(&s_cnt[(int)v], 1);
+        if (ok) {
+            atomicAdd(&s_cnt[(int)v], 1);
+            if (p < p0) atomicAdd(&s_before[(int)v], 1);
+        }
     }
     __syncthreads();
 
     // warp 0: exclusive prefix sum of the (aligned) counts, each lane a contiguous run
-    // of up to 32 experts, then a shuffle scan of the runs. Meanwhile warps 1..: ranks
-    // of this block's pairs (the number of earlier pairs with the same expert), every
-    // thread checking its share of the batch against up to 16 of the block's pairs at
-    // a time (sparse shared-memory atomics).
-    const int p0 = t_begin * a.k, q_end = nt * a.k;
+    // of up to 32 experts, then a shuffle scan of the runs. Meanwhile one thread per
+    // pair of this block: its rank inside its expert (the number of earlier pairs of
+    // the batch with the same expert) is the count before the block plus the block's
+    // own earlier pairs with that expert.
     if (warp == 0) {
         const int per = (a.E + 31) / 32;
         const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
@@ -174,22 +179,16 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
             s_total = incl;
             s_pairs = pairs;
         }
-    } else for (int g0 = 0; g0 < q_end; g0 += 16) {
-        int ge[16], cnt[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            ge[j] = g0 + j < q_end ? s_e[p0 + g0 + j] : -2;
-            cnt[j] = 0;
+    } else {
+        for (int q = tid - 32; q < q_end; q += kThreads - 32) {
+            const int e = s_e[p0 + q];
+            int r = 0;
+            if (e >= 0) {
+                r = s_before[e];
+                for (int q2 = 0; q2 < q; ++q2) r += s_e[p0 + q2] == e;
+            }
+            s_rank[q] = r;
         }
-        const int pmax = p0 + min(q_end, g0 + 16);
-        for (int pp = tid - 32; pp < pmax; pp += kThreads - 32) {
-            const int e = s_e[pp];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) cnt[j] += (e == ge[j]) & (pp < p0 + g0 + j);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)  // nearly every count is 0: sparse atomics
-            if (cnt[j]) atomicAdd(&s_rank[g0 + j], cnt[j]);
     }
     __syncthreads();
 

@@ -273,6 +273,18 @@ __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Barrier `id` (1..15; 0 is __syncthreads) over the first `threads` threads of the
+// block (a multiple of 32, whole warps, each of them calling it).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Arrival that publishes nothing: only "this block is running" (no ordering of the
+// block's earlier writes).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory variable in block `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
     uint32_t r;

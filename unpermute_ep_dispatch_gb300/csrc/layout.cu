@@ -156,8 +156,9 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     for (int e = tid; e < a.E; e += kThreads) rank_of[e] = e / a.epr;
     for (int r = tid; r < a.R; r += kThreads) node_of[r] = r / a.rpn;
     // cluster: this block has started; the other blocks store into its shared memory
-    // only once every block has arrived here
-    if constexpr (kCluster) cluster_arrive_release();
+    // only once every block has arrived here (nothing written so far is read by
+    // another block, so the arrival orders no writes)
+    if constexpr (kCluster) cluster_arrive_relaxed();
     // The tile ticket is taken before the dependency wait. It wraps to 0 by itself once
     // all `tiles` tickets of a call are handed out, and the next kernel on the stream
     // can only start once every block of this one has taken its ticket (the trigger
@@ -491,7 +492,76 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         }
     }
 
-    // (7) rank of every pair inside its expert over the whole batch
+    // (7) the last tile (in ticket order, or the cluster's last block) holds the
+    // totals. For E <= 1024 the first 8 warps write them while the others store the
+    // pair ranks: each of their 256 threads owns a contiguous run of experts (their
+    // counts, their sum P and, for the fused step 2, the exclusive prefix sum of the
+    // padded counts by a shuffle scan of the runs, then of the 8 warps' sums, between
+    // barriers of those 8 warps only); warp 8 writes the per-rank and per-node counts.
+    const bool last = tile == a.tiles - 1;
+    const bool warp_totals = a.E <= 1024;  // W >= 16 warps
+    auto padded = [&](int c) {
+        return a.alignment == 1 ? c : (c + a.alignment - 1) / a.alignment * a.alignment;
+    };
+    if (last && warp_totals && warp < 8) {
+        const int per = (a.E + 255) >> 8;
+        const int e0 = min(a.E, tid * per), e1 = min(a.E, e0 + per);
+        int part = 0, run = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int tot = col_excl[e] + col_agg[e];
+            if (a.per_expert) a.per_expert[e] = tot;
+            a.ws_counts[e] = tot;
+            part += tot;
+            run += padded(tot);
+        }
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        part = warp_sum(part);
+        if (lane == 31) {
+            s_red[warp] = incl;
+            s_red2[warp] = part;
+        }
+        named_barrier_sync(1, 256);
+        if (warp == 0) {
+            const int v = lane < 8 ? s_red[lane] : 0;
+            int wincl = v;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, wincl, o);
+                if (lane >= o) wincl += n;
+            }
+            const int P = warp_sum(lane < 8 ? s_red2[lane] : 0);
+            if (lane < 8) s_red[lane] = wincl - v;
+            if (lane == 7) {
+                a.hdr->total_pairs = P;
+                a.hdr->num_tokens = a.T;
+                a.hdr->num_topk = a.k;
+                if (a.start_out) *a.total_out = wincl;
+            }
+        }
+        if (a.start_out) {
+            named_barrier_sync(1, 256);
+            int pos = s_red[warp] + incl - run;
+            for (int e = e0; e < e1; ++e) {
+                a.start_out[e] = pos;
+                pos += padded(col_excl[e] + col_agg[e]);
+            }
+        }
+    } else if (last && warp_totals && warp == 8) {
+        for (int c = a.E + lane; c < a.cols; c += 32) {
+            const int tot = col_excl[c] + col_agg[c];
+            if (c < a.E + a.R) {
+                if (a.per_rank) a.per_rank[c - a.E] = tot;
+            }
+            else if (a.per_node) a.per_node[c - a.E - a.R] = tot;
+        }
+    }
+
+    // (8) rank of every pair inside its expert over the whole batch
     const int *my_base = hw + warp * hws;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
@@ -502,11 +572,10 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         }
     }
 
-    // (8) the last tile in ticket order holds the totals. Each thread owns a
-    // contiguous run of experts: their counts, their sum (P) and, for the fused
-    // step 2, the exclusive prefix sum of the (padded) counts by a warp-shuffle scan
-    // of the runs and then of the warps' sums.
-    if (tile == a.tiles - 1) {
+    // (8') the totals for E > 1024 (blocks of 4 or 8 warps): each thread owns a
+    // contiguous run of experts; a warp-shuffle scan of the runs, then of the warps'
+    // sums
+    if (last && !warp_totals) {
         const int per = (a.E + kThreads - 1) / kThreads;
         const int e0 = min(a.E, tid * per), e1 = min(a.E, e0 + per);
         int part = 0, run = 0;
@@ -515,7 +584,7 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
             if (a.per_expert) a.per_expert[e] = tot;
             a.ws_counts[e] = tot;
             part += tot;
-            run += a.alignment == 1 ? tot : (tot + a.alignment - 1) / a.alignment * a.alignment;
+            run += padded(tot);
         }
         for (int c = a.E + tid; c < a.cols; c += kThreads) {
             const int tot = col_excl[c] + col_agg[c];
@@ -558,8 +627,7 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
             int pos = s_red[warp] + incl - run;
             for (int e = e0; e < e1; ++e) {
                 a.start_out[e] = pos;
-                const int tot = col_excl[e] + col_agg[e];
-                pos += a.alignment == 1 ? tot : (tot + a.alignment - 1) / a.alignment * a.alignment;
+                pos += padded(col_excl[e] + col_agg[e]);
             }
         }
     }
@@ -567,12 +635,14 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // (9) the last block to finish advances the call counter for the next call (which
     // reads it only after its dependency wait, once this call has completed); the
     // finished-block count wraps back to 0 by itself
-    __syncthreads();
-    if (tid == 0 && multi) {
-        const unsigned prev = atomicInc(&a.hdr->done, (unsigned)(a.tiles - 1));
-        if (prev == (unsigned)a.tiles - 1) {
-            a.hdr->epoch = epoch + 1;
-            __threadfence();
+    if (multi) {
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned prev = atomicInc(&a.hdr->done, (unsigned)(a.tiles - 1));
+            if (prev == (unsigned)a.tiles - 1) {
+                a.hdr->epoch = epoch + 1;
+                __threadfence();
+            }
         }
     }
 }

@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kThreads) lowlatency_kernel(LLArgs a) {
 // ep_dispatch_lowlatency for a decode-sized batch: no layout kernel. Blocks
 // (x, y) share the token run x: every one reads the batch's picks into shared
 // memory and ranks the run's pairs (the number of earlier pairs, in row-major
-// order, with the same expert), which is all a fixed rectangle needs; it
+// order, with the same expert: the picks before the run are counted per expert as
+// they are parked), which is all a fixed rectangle needs; it
 // bulk-loads the run's bf16 rows into shared memory as it starts and casts the
 // units (token, two 128-column blocks) u = y, y + gridDim.y, ... from there. Blocks
 // with y = 0 write output_index and src_token; block (0, 0) counts the view's
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs 
     extern __shared__ __align__(128) uint8_t s_x[];  // the block's bf16 rows
     __shared__ int16_t s_e[kLLSmallPairs];
     __shared__ int s_cnt[kLLSmallExperts];            // block 0: picks per expert of the view
+    __shared__ int s_before[kLLSmallExperts];         // picks per expert before the run's first
     __shared__ int s_rank[kLLSmallBlockPairs], s_row[kLLSmallBlockPairs];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ int s_ok;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs 
     const bool first = lead && blockIdx.x == 0;         // writes recv_count
     if (first)
         for (int e = tid; e < EV; e += kThreads) s_cnt[e] = 0;
-    for (int q = tid; q < kLLSmallBlockPairs; q += kThreads) s_rank[q] = 0;
+    for (int e = tid; e < a.E; e += kThreads) s_before[e] = 0;
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         mbar_init_fence();
@@ -235,7 +237,9 @@ __global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs 
             bulk_load(s_x + tl * stride, a.x + (int64_t)(t_begin + tl) * bytes, bytes, &s_bar);
     }
     // the batch's picks: all of a thread's loads are issued first (one round trip),
-    // then parked in shared memory
+    // then parked in shared memory; those before the run's first pair are counted per
+    // expert (the base of the run's ranks)
+    const int p0 = t_begin * a.k, q_end = nt * a.k;
     constexpr int kPicksPerThread = kLLSmallPairs / kThreads;
     int64_t pv[kPicksPerThread];
 #pragma unroll
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs 
         const bool ok = v >= 0 && v < a.E;
         if ((v < -1 || v >= a.E) && first) report(a.status, EPD_ERR_INVALID_EXPERT);
         s_e[p] = ok ? (int16_t)v : (int16_t)-1;
+        if (ok && p < p0) atomicAdd(&s_before[(int)v], 1);
     }
     __syncthreads();
     if (first)
@@ -258,26 +263,16 @@ __global__ void __launch_bounds__(kThreads) lowlatency_small_kernel(LLSmallArgs 
             const int e = s_e[p];
             if (e >= a.e_begin && e < a.e_end) atomicAdd(&s_cnt[e - a.e_begin], 1);
         }
-    // ranks of this block's pairs: every thread checks its share of the batch against
-    // up to 16 of the block's pairs at a time (sparse shared-memory atomics)
-    const int p0 = t_begin * a.k, q_end = nt * a.k;
-    for (int g0 = 0; g0 < q_end; g0 += 16) {
-        int ge[16], cnt[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int e = g0 + j < q_end ? s_e[p0 + g0 + j] : -2;
-            ge[j] = (e >= a.e_begin && e < a.e_end) ? e : -2;  // only the view's picks get rows
-            cnt[j] = 0;
+    // ranks of the run's pairs (the view's picks only get rows): the count before the
+    // run plus the run's own earlier pairs with the same expert
+    for (int q = tid; q < q_end; q += kThreads) {
+        const int e = s_e[p0 + q];
+        int r = 0;
+        if (e >= a.e_begin && e < a.e_end) {
+            r = s_before[e];
+            for (int q2 = 0; q2 < q; ++q2) r += s_e[p0 + q2] == e;
         }
-        const int pmax = p0 + min(q_end, g0 + 16);
-        for (int pp = tid; pp < pmax; pp += kThreads) {
-            const int e = s_e[pp];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) cnt[j] += (e == ge[j]) & (pp < p0 + g0 + j);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (cnt[j]) atomicAdd(&s_rank[g0 + j], cnt[j]);
+        s_rank[q] = r;
     }
     __syncthreads();
     // rows in the rectangles; a pick past its rectangle is dropped and reported
