@@ -139,16 +139,6 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     __shared__ int s_red[W], s_red2[W];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    {  // zero the warp histograms, 16 bytes per store (the region is 16-byte aligned)
-        const int n4 = (W * hws) >> 2;
-        int4 *hw4 = reinterpret_cast<int4 *>(hw);
-        for (int i = tid; i < n4; i += kThreads) hw4[i] = make_int4(0, 0, 0, 0);
-        for (int i = 4 * n4 + tid; i < W * hws; i += kThreads) hw[i] = 0;
-        const int m4 = kLaneWords ? (W * a.E) >> 2 : 0;  // the lane masks, likewise
-        int4 *lm4 = reinterpret_cast<int4 *>(lanes_of);
-        for (int i = tid; i < m4; i += kThreads) lm4[i] = make_int4(0, 0, 0, 0);
-        for (int i = 4 * m4 + tid; kLaneWords && i < W * a.E; i += kThreads) lanes_of[i] = 0u;
-    }
     for (int i = tid; i < a.cols_pad; i += kThreads) {
         col_agg[i] = 0;
         col_excl[i] = 0;
@@ -193,11 +183,19 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     const int cpw = max(1, min(kChunks, (npairs + kThreads - 1) / kThreads));
     const int p_base = warp * 32 * cpw + lane;
     const int live = min(cpw, max(0, (npairs - (p_base - lane) + 31) >> 5));
+    int64_t pv[kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int p = p_base + 32 * c;
-        int64_t v = -1;
-        if (c < cpw && p < npairs) v = __ldg(a.topk + pair0 + p);
+        pv[c] = (c < cpw && p < npairs) ? __ldg(a.topk + pair0 + p) : -1;
+    }
+    // while the picks are in flight, the warp zeroes its own histogram row (the lane
+    // words need no zeroing: each chunk clears the words it uses before setting them)
+    int *my_hist = hw + warp * hws;
+    for (int i = lane; i < hws; i += 32) my_hist[i] = 0;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const int64_t v = pv[c];
         pe[c] = (v >= 0 && v < a.E) ? (int)v : -1;
         if (v < -1 || v >= a.E) report(a.status, EPD_ERR_INVALID_EXPERT);
     }
@@ -207,20 +205,23 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         const int p = p_base + 32 * c;
         if (c < live && p < npairs) s_pick[p] = (int16_t)pe[c];
     }
-    int *my_hist = hw + warp * hws;
     uint32_t *my_lanes = lanes_of + warp * a.E;
+    __syncwarp();  // the row is zero for every lane of the warp
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         pr[c] = 0;
         if (c >= live) continue;
         const int e = pe[c];
-        // the lanes holding the same expert: every lane sets its bit in the expert's
-        // word, then reads the word back (a shared-memory atomic OR and a load cost a
-        // fraction of the one-ballot-per-id-bit search they replace); every lane reads
-        // the group's count before the group's lowest lane adds to it and clears the
-        // word for the next chunk; the warp stays converged (whole-warp syncs only)
+        // the lanes holding the same expert: every lane clears the expert's word, then
+        // sets its bit in it, then reads the word back (a shared-memory atomic OR and a
+        // load cost a fraction of the one-ballot-per-id-bit search they replace); every
+        // lane reads the group's count before the group's lowest lane adds to it; the
+        // warp stays converged (whole-warp syncs only). The syncs of the next chunk
+        // order its reads after this chunk's count update.
         uint32_t peers;
         if constexpr (kLaneWords) {
+            if (e >= 0) my_lanes[e] = 0u;
+            __syncwarp();
             if (e >= 0) atomicOr(&my_lanes[e], 1u << lane);
             __syncwarp();
             peers = e >= 0 ? my_lanes[e] : 0u;
@@ -237,11 +238,8 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         const int base = e >= 0 ? my_hist[e] : 0;
         pr[c] = base + before;
         __syncwarp();
-        if (e >= 0 && before == 0) {
-            my_hist[e] = base + __popc(peers);
-            if constexpr (kLaneWords) my_lanes[e] = 0u;
-        }
-        __syncwarp();
+        if (e >= 0 && before == 0) my_hist[e] = base + __popc(peers);
+        if constexpr (!kLaneWords) __syncwarp();
     }
 
     __syncthreads();
