@@ -106,7 +106,9 @@ EPD_API int epd_last_cuda_error(void);
  * picks, E experts, R ranks and N nodes. The workspace holds the per-pair rank
  * inside its expert (T*k int32), the per-expert counts and, for batches beyond
  * one thread-block cluster, the per-tile state of the layout's single-pass
- * look-back. Returns 0 for invalid sizes. Host-only arithmetic.
+ * look-back (whose count rows, when the batch runs as several clusters, hold the
+ * counts each cluster publishes). Returns 0 for invalid sizes. Host-only
+ * arithmetic.
  */
 EPD_API size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                            int num_rdma_ranks);
@@ -114,8 +116,9 @@ EPD_API size_t epd_workspace_bytes(int num_tokens, int num_topk, int num_experts
 /*
  * Zero-fills `workspace` (device, `bytes` long) on `stream`. A workspace must
  * be zero-filled once before its first use; the layout call keeps it reusable
- * from then on, for calls of any shape that fits (its look-back state words are
- * tagged with a call counter and a mark no other workspace data carries). A
+ * from then on, for calls of any shape that fits (its look-back state words and
+ * the counts clusters publish are tagged with a call counter and a mark no other
+ * workspace data carries). A
  * workspace serves one stream at a time: calls on different streams that
  * overlap on the GPU and share a workspace race.
  */
@@ -136,9 +139,12 @@ EPD_API epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_strea
  * every pair among the pairs of its expert in token-major (t, then j) order,
  * which ep_permute turns into slots. The ranks come from per-tile counts and
  * an exclusive prefix over token tiles: for up to 16 x 8192 pairs (E <= 1024)
- * the tiles are the 2-16 blocks of one thread-block cluster, which exchange
- * their counts through distributed shared memory; larger batches use a
- * single-pass decoupled look-back over tiles taken in ticket order. Either way
+ * the tiles are the blocks of thread-block clusters of 2-16 blocks, which
+ * exchange their counts through distributed shared memory -- one cluster, or,
+ * where one cluster of 16 would need 8 chunks of 32 pairs per warp, up to 8
+ * clusters that all fit on the device at once, whose last blocks publish each
+ * cluster's counts in the workspace for the later clusters; larger batches use
+ * a single-pass decoupled look-back over tiles taken in ticket order. Every way
  * the result does not depend on the order in which blocks run. Ids outside
  * [-1, E) set EPD_ERR_INVALID_EXPERT in *status and are treated as -1.
  */

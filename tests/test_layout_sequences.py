@@ -6,12 +6,14 @@ calls are issued back to back on one stream and one workspace, with different
 topk_idx and nothing in between, and each call's outputs are compared element by
 element with the oracle -- the counts, masks and offsets, and the second call's
 per-pair ranks through the permute that follows it (output_index, m_indices).
-Sizes span the cluster form (dsv3: 16 blocks) and the tile form with its
-ticket and look-back (524 288 pairs: 128 tiles of 4096 pairs).
+Sizes span the cluster form (dsv3: one cluster of 16 blocks), several clusters
+(131 072 pairs: their counts meet through global memory) and the tile form with
+its ticket and look-back (524 288 pairs: 128 tiles of 4096 pairs).
 
-A second group plants leftovers in the look-back state region of a workspace
-(values an earlier call of another shape, or an earlier call, leaves there) and
-checks that the next call ignores them.
+A second group plants leftovers in the look-back state region of a workspace, or
+in the region where several clusters publish their counts (values an earlier call
+of another shape, or an earlier call, leaves there) and checks that the next call
+ignores them.
 """
 import numpy as np
 import pytest
@@ -98,7 +100,7 @@ PAIRS = [("layout", "layout"), ("layout", "offsets"), ("offsets", "layout"),
 
 
 @pytest.mark.parametrize("first,second", PAIRS)
-@pytest.mark.parametrize("T,k", [(8192, 8), (65536, 8)])
+@pytest.mark.parametrize("T,k", [(8192, 8), (16384, 8), (65536, 8)])
 def test_two_layout_calls_back_to_back(first, second, T, k):
     dev = torch.device("cuda")
     a, b = _case(T, k, seed=T + 1), _case(T, k, seed=T + 2, routing="repeats")
@@ -225,11 +227,57 @@ def test_leftover_state_words_are_ignored(plant):
     _check_ranks(small, ws, st, os_.start, f"after planting {plant}")
 
 
+def _cluster_region(T, k):
+    """Byte offset of the words several clusters publish their counts in: the tile
+    form's aggregate rows, after the state words (256-byte aligned)."""
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    state_off, tiles = _state_region(T, k)
+    return up(state_off + 8 * tiles)
+
+
+@pytest.mark.parametrize("plant", ["small_ints", "previous_call_tags", "minus_one"])
+def test_leftover_cluster_words_are_ignored(plant):
+    """131 072 pairs run as several clusters, whose last blocks publish each
+    cluster's counts as self-tagged 64-bit words. Leftovers planted over those words
+    between two calls -- small 32-bit values, words tagged with the previous call's
+    counter, -1 everywhere -- are not taken for this call's counts."""
+    dev = torch.device("cuda")
+    T, k = 16384, 8
+    a = _case(T, k, seed=61)
+    b = _case(T, k, seed=62, routing="repeats")
+    ws = epd.new_workspace(T, k, E, R, N, dev)
+    st = epd.new_status(dev)
+    oa, ob = Outs(T, dev), Outs(T, dev)
+    _launch("offsets", a.topk_idx.to(dev), ws, st, oa)
+    torch.cuda.synchronize()
+    epoch = int(ws[8:16].view(torch.int64).item())
+    assert epoch >= 1                                   # the call ran as several clusters
+    off = _cluster_region(T, k)
+    n = 8 * 320                                          # 8 clusters x padded columns
+    words = ws[off: off + 8 * n].view(torch.int64)
+    if plant == "small_ints":
+        ws[off: off + 8 * n].view(torch.int32).copy_(
+            torch.arange(2 * n, dtype=torch.int32, device=dev) % 7 + 1)
+    elif plant == "previous_call_tags":
+        prev = (1 << 63) | (((epoch - 1) & ((1 << 42) - 1)) << 21) | 12345
+        words.fill_(prev - (1 << 64))
+    else:
+        words.fill_(-1)
+    _launch("offsets", b.topk_idx.to(dev), ws, st, ob)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert int(ws[8:16].view(torch.int64).item()) == epoch + 1
+    _check_layout("offsets", a, oa, "first call")
+    _check_layout("offsets", b, ob, f"after planting {plant}")
+    _check_ranks(b, ws, st, ob.start, f"after planting {plant}")
+
+
 # ----------------------------------------------------------------------------- the two layout forms
 # Batches of up to 16 x 8192 (token, pick) pairs (E <= 1024, <= 2048 tokens per block)
-# run the cluster form; larger ones the tile form. Each case below sits on an edge of
-# that choice or of the cluster form itself, and the whole path is compared with the
-# oracle (counts, masks, offsets, slots, rows, combine).
+# run the cluster form -- as several clusters where one cluster of 16 blocks would need
+# eight chunks per warp -- and larger ones the tile form. Each case below sits on an
+# edge of those choices or of the forms themselves, and the whole path is compared
+# with the oracle (counts, masks, offsets, slots, rows, combine).
 FORM_EDGES = [
     # T, k, E, R, N
     (129, 64, 16, 8, 2),        # 16 blocks; the last one holds no token
@@ -241,6 +289,10 @@ FORM_EDGES = [
     (32769, 1, 256, 32, 4),     # one token over it: the tile form
     (16385, 8, 256, 32, 4),     # one token over the cluster's pairs: the tile form
     (1025, 1, 16, 8, 2),        # just over one tile: a cluster of two
+    (8200, 8, 256, 32, 4),      # just over 16 x 4096 pairs: several clusters
+    (9000, 8, 256, 32, 4),      # several clusters, the last tiles of the last one empty
+    (16384, 8, 256, 32, 4),     # several clusters at the cluster form's largest batch
+    (4000, 16, 1024, 32, 4),    # several clusters of 16-warp blocks (E > 512)
 ]
 
 

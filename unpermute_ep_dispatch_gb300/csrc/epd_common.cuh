@@ -213,6 +213,10 @@ __device__ __forceinline__ void st_release_gpu(uint64_t *p, uint64_t v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_relaxed_gpu(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
     uint64_t v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -255,6 +259,13 @@ __device__ __forceinline__ int bit_column_count(uint32_t x, int lane) {
 __device__ __forceinline__ int spread4(uint32_t b) { return (int)(((b & 0xFu) * 0x00204081u) & 0x01010101u); }
 
 // ---------------------------------------------------------------------------- thread-block clusters
+// Index of this block's cluster in the grid (x).
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
 // Rank of this block inside its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

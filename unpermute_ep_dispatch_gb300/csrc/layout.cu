@@ -51,6 +51,16 @@ constexpr uint64_t kStateMark = 1ull << 63;
 constexpr uint32_t kStateAgg = 1;   // tile published its own counts
 constexpr uint32_t kStateIncl = 2;  // tile published counts of itself and all earlier tiles
 constexpr uint32_t kDefaultSpinLimit = 1u << 19;  // polls with back-off: about a second
+// A cluster's published count (several clusters): kStateMark | call counter << 21 |
+// count. Counts stay below 2^21 (the form is used for at most 2^20 pairs) and the
+// call counter keeps 42 bits. Leftovers never read as current: an int32 pair whose
+// upper word is >= 0 lacks the mark, one whose upper word is -1 would need a counter
+// with its 31 top bits set, and an earlier call's word carries another counter
+// unless 2^42 calls lie between them.
+constexpr int kAggValueBits = 21;
+constexpr uint64_t kAggValueMask = (1ull << kAggValueBits) - 1;
+constexpr uint64_t kAggEpochMask = (1ull << 42) - 1;
+constexpr int kMaxClusters = 8;
 
 struct LayoutArgs {
     const int64_t *topk;
@@ -63,6 +73,8 @@ struct LayoutArgs {
     uint64_t *state;
     int32_t *agg, *incl;
     int tiles, tile_tokens, cols, cols_pad;
+    int csize, ccount;  // cluster form: blocks per cluster and clusters (tiles = csize * ccount)
+    uint64_t *gagg;     // cluster form, ccount > 1: [ccount][cols_pad] published cluster counts
     int rank_shift, node_shift;  // log2(E/R), log2(R/N) when powers of two, else -1
     int32_t *start_out;  // optional: expert offsets written by the last tile (fused step 2)
     int32_t *total_out;
@@ -79,11 +91,14 @@ __device__ __forceinline__ int warp_sum(int v) {
 }
 
 // kChunks: 32-pair chunks per warp at most (a tile holds up to W * 32 * kChunks pairs).
-// kCluster: the tiles are the blocks of one thread-block cluster, all running at
-// once; each block pushes its counts into the shared memory of every later block
-// of the cluster and one cluster barrier completes every prefix (no ticket, no
-// look-back through global memory). Otherwise tiles are handed out by ticket and
-// chained by the decoupled look-back.
+// kForm 1 (one cluster) and 2 (several): the tiles are the blocks of thread-block
+// clusters that all run at once (tile = cluster index * blocks per cluster + rank in
+// the cluster); each block pushes its counts into the shared memory of every later
+// block of its cluster and one cluster barrier completes every prefix inside the
+// cluster (no ticket). With several clusters, each cluster's last block then
+// publishes the cluster's counts in global memory (self-tagged 64-bit words) and the
+// blocks of later clusters add those of the clusters before theirs. kForm 0: tiles
+// are handed out by ticket and chained by the decoupled look-back.
 // Byte offsets of the layout kernel's shared-memory regions; every region that is
 // read or written with 16-byte vectors starts on a 16-byte boundary.
 struct LayoutSmem {
@@ -107,9 +122,10 @@ __host__ __device__ inline LayoutSmem layout_smem(int E, int W, int cols_pad, in
     return m;
 }
 
-template <int W, int kChunks, bool kCluster>
+template <int W, int kChunks, int kForm>
 __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     constexpr int kThreads = W * 32;
+    constexpr bool kCluster = kForm >= 1, kMulti = kForm == 2;
     // lane-mask words per warp and expert for E <= 1024 (16 or 32 warps); wider
     // expert sets keep their shared memory for the histograms and use ballots
     constexpr bool kLaneWords = W >= 16;
@@ -159,13 +175,17 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // call has completed. A call with one tile needs none of it (no look-back).
     const bool multi = !kCluster && a.tiles > 1;  // ticket, look-back and call counter
     if (tid == 0)
-        s_tile = kCluster ? (int)cluster_ctarank()
-                          : multi ? (int)atomicInc(&a.hdr->ticket, (unsigned)(a.tiles - 1)) : 0;
+        s_tile = kMulti ? (int)(cluster_id_x() * a.csize + cluster_ctarank())
+                 : kCluster ? (int)cluster_ctarank()
+                 : multi ? (int)atomicInc(&a.hdr->ticket, (unsigned)(a.tiles - 1)) : 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    if (tid == 0) s_epoch = multi ? ld_relaxed_gpu(&a.hdr->epoch) : 0ull;
+    // the call counter, read before this block's cluster barrier: once a cluster's
+    // counts are published, every block of that cluster has read it
+    if (tid == 0) s_epoch = (multi || kMulti) ? ld_relaxed_gpu(&a.hdr->epoch) : 0ull;
     const int tile = s_tile;
+    const int crank = kMulti ? tile % a.csize : tile;  // rank inside the cluster
     const int t0 = tile * a.tile_tokens;
     const int ntok = max(0, min(a.tile_tokens, a.T - t0));
     const int npairs = ntok * a.k;
@@ -318,20 +338,20 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
         // vectors, into row `tile` of the staging area of every later block -- the expert
         // columns to each of them, all columns to the last one (which writes the totals)
         cluster_wait_acquire();
-        const int later = a.tiles - 1 - tile;
+        const int later = a.csize - 1 - crank;
         const int nv_e = (a.E + 3) >> 2, nv_all = a.cols_pad >> 2;
         const int n_mid = later > 0 ? (later - 1) * nv_e : 0;
         const int n_send = later > 0 ? n_mid + nv_all : 0;
         const int4 *row = reinterpret_cast<const int4 *>(col_agg);
-        int *dst_row = s_stage + tile * a.cols_pad;
+        int *dst_row = s_stage + crank * a.cols_pad;
         for (int i = tid; i < n_send; i += kThreads) {
             int d, v;
             if (i < n_mid) {
                 d = i / nv_e;
                 v = i - d * nv_e;
-                d += tile + 1;
+                d += crank + 1;
             } else {
-                d = a.tiles - 1;
+                d = a.csize - 1;
                 v = i - n_mid;
             }
             cluster_st_v4(cluster_map(dst_row + 4 * v, (uint32_t)d), row[v]);
@@ -407,13 +427,59 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // this tile is the sum of the rows of the earlier tiles
     if constexpr (kCluster) {
         cluster_wait_acquire();
-        const int ncol = tile == a.tiles - 1 ? a.cols : a.E;
+        const int ncol = crank == a.csize - 1 ? a.cols : a.E;
         for (int c = tid; c < ncol; c += kThreads) {
             int sum = 0;
-            for (int t = 0; t < tile; ++t) sum += s_stage[t * a.cols_pad + c];
+            for (int t = 0; t < crank; ++t) sum += s_stage[t * a.cols_pad + c];
             col_excl[c] = sum;
         }
         __syncthreads();
+        if constexpr (kMulti) {
+            // several clusters: the last block of every cluster but the last publishes
+            // the cluster's counts (all columns); the blocks of cluster g add those of
+            // clusters 0..g-1 to their prefixes (all columns for the grid's last block,
+            // which writes the totals), loading every word at once and polling again,
+            // bounded, only where a cluster has not published yet
+            const int cid = tile / a.csize;
+            const uint64_t mark = kStateMark | ((s_epoch & kAggEpochMask) << kAggValueBits);
+            if (crank == a.csize - 1 && cid < a.ccount - 1) {
+                uint64_t *mine = a.gagg + (size_t)cid * a.cols_pad;
+                for (int c = tid; c < a.cols; c += kThreads)
+                    st_relaxed_gpu(&mine[c], mark | (uint64_t)(uint32_t)(col_excl[c] + col_agg[c]));
+            }
+            if (cid > 0) {
+                const int ncol2 = tile == a.tiles - 1 ? a.cols : a.E;
+                for (int c = tid; c < ncol2; c += kThreads) {
+                    uint64_t v[kMaxClusters - 1];
+#pragma unroll
+                    for (int g = 0; g < kMaxClusters - 1; ++g)
+                        v[g] = g < cid ? ld_relaxed_gpu(a.gagg + (size_t)g * a.cols_pad + c) : mark;
+                    int sum = 0;
+#pragma unroll
+                    for (int g = 0; g < kMaxClusters - 1; ++g) {
+                        if (g >= cid) break;
+                        uint32_t polls = 0;
+                        unsigned ns = 32;
+                        while ((v[g] & ~kAggValueMask) != mark) {
+                            if (++polls >= a.spin_limit) {
+                                report(a.status, EPD_ERR_TIMEOUT);
+                                v[g] = mark;
+                                break;
+                            }
+                            __nanosleep(ns);
+                            if (ns < 256) ns <<= 1;
+                            v[g] = ld_relaxed_gpu(a.gagg + (size_t)g * a.cols_pad + c);
+                        }
+                        sum += (int)(v[g] & kAggValueMask);
+                    }
+                    col_excl[c] += sum;
+                }
+            }
+            __syncthreads();
+            // every block of the call has read the call counter (the clusters before
+            // published, this cluster passed its barrier): advance it for the next call
+            if (tile == a.tiles - 1 && tid == 0) a.hdr->epoch = s_epoch + 1;
+        }
     }
 
     // (5) decoupled look-back over earlier tiles
@@ -674,29 +740,30 @@ epd_status_t opt_in_smem(K kernel, size_t smem) {
 
 template <int W, int CH>
 epd_status_t launch_tiles(const LayoutArgs &a, size_t smem, cudaStream_t stream) {
-    auto kernel = layout_kernel<W, CH, false>;
+    auto kernel = layout_kernel<W, CH, 0>;
     const epd_status_t st = opt_in_smem(kernel, smem);
     if (st != EPD_OK) return st;
     return launch_pdl(kernel, a.tiles, W * 32, smem, stream, a);
 }
 
-// Whether a cluster of C blocks of layout_kernel<W, CH, true> with `smem` bytes each can
-// run on the current device (the answer for the last size asked is kept per device).
-template <int W, int CH>
-bool cluster_fits(int C, size_t smem) {
-    static std::atomic<unsigned long long> last[64][2];  // (smem << 1 | fits) + 1, 0 = unknown
-    auto kernel = layout_kernel<W, CH, true>;
+// How many clusters of C blocks of layout_kernel<W, CH, F> with `smem` bytes each
+// can run at once on the current device, 0 if none (the answer for the last size
+// asked is kept per device and cluster width).
+template <int W, int CH, int F>
+int cluster_capacity(int C, size_t smem) {
+    static std::atomic<unsigned long long> last[64][2];  // (smem << 8 | count) + 1, 0 = unknown
+    auto kernel = layout_kernel<W, CH, F>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return 0;
     }
     const int slot = C > 8 ? 1 : 0;
     std::atomic<unsigned long long> *cache =
         (dev >= 0 && dev < 64) ? &last[dev][slot] : nullptr;
     if (cache) {
         const unsigned long long v = cache->load(std::memory_order_acquire);
-        if (v != 0 && ((v - 1) >> 1) == smem) return ((v - 1) & 1) != 0;
+        if (v != 0 && ((v - 1) >> 8) == smem) return (int)((v - 1) & 0xffu);
     }
     bool fits = opt_in_smem(kernel, smem) == EPD_OK;
     if (fits && C > 8 &&
@@ -704,6 +771,7 @@ bool cluster_fits(int C, size_t smem) {
         cudaGetLastError();
         fits = false;
     }
+    int n = 0;
     if (fits) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)C);
@@ -716,55 +784,82 @@ bool cluster_fits(int C, size_t smem) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
-        fits = n >= 1;
     }
-    if (cache) cache->store(((unsigned long long)smem << 1 | (fits ? 1ull : 0ull)) + 1,
+    n = n < 0 ? 0 : (n > 255 ? 255 : n);
+    if (cache) cache->store(((unsigned long long)smem << 8 | (unsigned)n) + 1,
                             std::memory_order_release);
-    return fits;
+    return n;
 }
 
-template <int W, int CH>
+template <int W, int CH, int F>
 epd_status_t launch_cluster(const LayoutArgs &a, size_t smem, cudaStream_t stream) {
-    return launch_pdl_cluster(layout_kernel<W, CH, true>, a.tiles, W * 32, smem, a.tiles, stream,
-                              a);
+    return launch_pdl_cluster(layout_kernel<W, CH, F>, a.tiles, W * 32, smem, a.csize, stream, a);
 }
 
-template <int W>
-bool cluster_fits_any(int CH, int C, size_t smem) {
+// Form F = 1 (one cluster) takes 1..8 chunks per warp; F = 2 (several clusters) 1..4.
+template <int W, int F>
+int cluster_capacity_any(int CH, int C, size_t smem) {
     switch (CH) {
-        case 1: return cluster_fits<W, 1>(C, smem);
-        case 2: return cluster_fits<W, 2>(C, smem);
-        case 4: return cluster_fits<W, 4>(C, smem);
-        default: return cluster_fits<W, 8>(C, smem);
+        case 1: return cluster_capacity<W, 1, F>(C, smem);
+        case 2: return cluster_capacity<W, 2, F>(C, smem);
+        case 4: return cluster_capacity<W, 4, F>(C, smem);
+        default: return F == 1 ? cluster_capacity<W, 8, 1>(C, smem) : 0;
     }
 }
 
-template <int W>
+template <int W, int F>
 epd_status_t launch_cluster_any(int CH, const LayoutArgs &a, size_t smem, cudaStream_t stream) {
     switch (CH) {
-        case 1: return launch_cluster<W, 1>(a, smem, stream);
-        case 2: return launch_cluster<W, 2>(a, smem, stream);
-        case 4: return launch_cluster<W, 4>(a, smem, stream);
-        default: return launch_cluster<W, 8>(a, smem, stream);
+        case 1: return launch_cluster<W, 1, F>(a, smem, stream);
+        case 2: return launch_cluster<W, 2, F>(a, smem, stream);
+        case 4: return launch_cluster<W, 4, F>(a, smem, stream);
+        default: return F == 1 ? launch_cluster<W, 8, 1>(a, smem, stream) : EPD_ERR_UNSUPPORTED;
     }
 }
 
-// The cluster form for a batch of `pairs` (token, pick) pairs: the number of blocks
-// (a power of two, 2..16, about one per 1024 pairs) and the chunks per warp, or
-// C = 0 when the batch fits one tile, exceeds what one cluster holds, or the device
-// cannot co-schedule the cluster.
+// The cluster form for a batch of `pairs` (token, pick) pairs: blocks per cluster C (a
+// power of two, 2..16, about one block per 1024 pairs), clusters G and chunks per warp,
+// or C = 0 when the batch fits one tile, exceeds what the form holds, or the device
+// cannot co-schedule the clusters. A batch that would give one cluster of 16 blocks
+// kMultiMinChunks or more chunks per warp is spread over up to kMaxClusters clusters
+// that all fit on the device at once, one block per SM, when the workspace's
+// look-back rows (which then hold the clusters' published counts: 2 G rows of 32-bit
+// words) are enough.
 struct ClusterPlan {
-    int C, chunks, tile_tokens;
+    int C, G, chunks, tile_tokens;
     size_t smem;
 };
 
-ClusterPlan plan_cluster(int T, int k, int E, int cols_pad) {
-    ClusterPlan p = {0, 0, 0, 0};
+constexpr int kMultiMinChunks = 8;
+
+// Shared memory per block that keeps two of them off one SM (per device).
+size_t one_block_per_sm_smem() {
+    static std::atomic<int> by_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int v = (dev >= 0 && dev < 64) ? by_dev[dev].load(std::memory_order_acquire) : 0;
+    if (v == 0) {
+        int per_sm = 0;
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        v = (int)align_up((size_t)per_sm / 2 + 1024, 16);
+        if (dev >= 0 && dev < 64) by_dev[dev].store(v, std::memory_order_release);
+    }
+    return (size_t)v;
+}
+
+ClusterPlan plan_cluster(int T, int k, int E, int cols_pad, int ws_tiles) {
+    ClusterPlan p = {0, 1, 0, 0, 0};
     const int W = layout_warps(E);
     const int64_t pairs = (int64_t)T * k;
     if (W < 16 || pairs <= kLayoutTilePairs) return p;
@@ -777,14 +872,35 @@ ClusterPlan plan_cluster(int T, int k, int E, int cols_pad) {
         int ch = 1;
         while ((int64_t)ch * W * 32 < tp) ch *= 2;
         const size_t smem = layout_smem_bytes(E, cols_pad, tt, tp, C);
-        const bool fits = W == 32 ? cluster_fits_any<32>(ch, C, smem)
-                                  : cluster_fits_any<16>(ch, C, smem);
-        if (fits) {
+        const int n = W == 32 ? cluster_capacity_any<32, 1>(ch, C, smem)
+                              : cluster_capacity_any<16, 1>(ch, C, smem);
+        if (n >= 1) {
             p.C = C;
             p.chunks = ch;
             p.tile_tokens = tt;
             p.smem = smem;
-            return p;
+            break;
+        }
+    }
+    if (p.C != kMaxCluster || p.chunks < kMultiMinChunks || pairs >= (1ll << kAggValueBits))
+        return p;
+    const size_t one = one_block_per_sm_smem();
+    for (int G = p.chunks < kMaxClusters ? p.chunks : kMaxClusters; G >= 2; G /= 2) {
+        if (2 * G > ws_tiles) continue;
+        const int tt = (T + C * G - 1) / (C * G);
+        const int64_t tp = (int64_t)tt * k;
+        int ch = 1;
+        while ((int64_t)ch * W * 32 < tp) ch *= 2;
+        size_t smem = layout_smem_bytes(E, cols_pad, tt, tp, C);
+        if (smem < one) smem = one;
+        const int n = W == 32 ? cluster_capacity_any<32, 2>(ch, C, smem)
+                              : cluster_capacity_any<16, 2>(ch, C, smem);
+        if (n >= G) {
+            p.G = G;
+            p.chunks = ch;
+            p.tile_tokens = tt;
+            p.smem = smem;
+            break;
         }
     }
     return p;
@@ -844,13 +960,22 @@ epd_status_t layout_launch(int32_t *start_out, int32_t *total_out, int alignment
     a.stalled_tile = stalled_tile;
     a.spin_limit = spin_limit;
     // the failure-detection hook needs the look-back, so it always runs the tile form
-    const ClusterPlan cp = stalled_tile < 0 ? plan_cluster(T, k, E, w.cols_pad)
-                                            : ClusterPlan{0, 0, 0, 0};
+    a.csize = 1;
+    a.ccount = 1;
+    a.gagg = nullptr;
+    const ClusterPlan cp = stalled_tile < 0 ? plan_cluster(T, k, E, w.cols_pad, w.tiles)
+                                            : ClusterPlan{0, 1, 0, 0, 0};
     if (cp.C > 0) {
-        a.tiles = cp.C;
+        a.csize = cp.C;
+        a.ccount = cp.G;
+        a.tiles = cp.C * cp.G;
         a.tile_tokens = cp.tile_tokens;
-        return layout_warps(E) == 32 ? launch_cluster_any<32>(cp.chunks, a, cp.smem, stream)
-                                     : launch_cluster_any<16>(cp.chunks, a, cp.smem, stream);
+        a.gagg = reinterpret_cast<uint64_t *>(ws + w.agg_off);
+        if (cp.G > 1)
+            return layout_warps(E) == 32 ? launch_cluster_any<32, 2>(cp.chunks, a, cp.smem, stream)
+                                         : launch_cluster_any<16, 2>(cp.chunks, a, cp.smem, stream);
+        return layout_warps(E) == 32 ? launch_cluster_any<32, 1>(cp.chunks, a, cp.smem, stream)
+                                     : launch_cluster_any<16, 1>(cp.chunks, a, cp.smem, stream);
     }
     const size_t smem = layout_smem_bytes(E, w.cols_pad, a.tile_tokens,
                                           (int64_t)a.tile_tokens * k, 0);
