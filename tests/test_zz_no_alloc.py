@@ -97,16 +97,18 @@ def test_noalloc_binding_and_size_limit(lib):
 
 def test_noalloc_shape_changes_leave_no_stale_state(lib):
     """The shared array keeps each call's leftovers. A big call writes its pair ranks
-    where a smaller many-tile call keeps its look-back state words; the smaller call
-    must not read them as published states. Repeated, alternating shapes, each
-    result against the oracle."""
+    where a smaller call keeps its look-back state words or its clusters' published
+    counts; the smaller call must not read them as published. Repeated, alternating
+    shapes -- the tile form (320 000 pairs), several clusters (131 072 pairs) and one
+    cluster -- each result against the oracle."""
     import numpy as np
 
     import oracle
     dev = torch.device("cuda")
     stream = torch.cuda.current_stream(dev)
     E, R, N, k = 256, 32, 4, 8
-    shapes = [(8192, 301), (2048, 302), (4096, 303), (1100, 304)]   # (T, seed)
+    shapes = [(40000, 305), (8192, 301), (16384, 306), (2048, 302), (4096, 303),
+              (1100, 304)]                                          # (T, seed)
     cases = [workloads.make_random_case(T=T, H=16, k=k, E=E, R=R, N=N, dtype="bf16", seed=s,
                                         routing="repeats", p_invalid=0.05, experts="identity")
              for T, s in shapes]
@@ -115,7 +117,7 @@ def test_noalloc_shape_changes_leave_no_stale_state(lib):
     st = epd.new_status(dev)
     for rep in range(100):
         outs = []
-        for c, topk in zip(cases, tops):            # four calls back to back, then one sync
+        for c, topk in zip(cases, tops):            # six calls back to back, then one sync
             o = _outputs(c.T, E, R, N, dev, -3)
             per_e, per_r, per_n, itr = o
             rc = lib.ep_dispatch_layout_noalloc(
