@@ -143,7 +143,9 @@ EPD_API epd_status_t epd_workspace_init(void *workspace, size_t bytes, epd_strea
  * exchange their counts through distributed shared memory -- one cluster, or,
  * where one cluster of 16 would need 8 chunks of 32 pairs per warp, up to 8
  * clusters that all fit on the device at once, whose last blocks publish each
- * cluster's counts in the workspace for the later clusters; larger batches use
+ * cluster's counts in the workspace for the later clusters (a later cluster waits
+ * for the earlier ones to run: should other work hold the SMs they need for about
+ * a second, the wait gives up with EPD_ERR_TIMEOUT); larger batches use
  * a single-pass decoupled look-back over tiles taken in ticket order. Every way
  * the result does not depend on the order in which blocks run. Ids outside
  * [-1, E) set EPD_ERR_INVALID_EXPERT in *status and are treated as -1.
