@@ -306,3 +306,37 @@ def test_layout_form_edges(T, k, E, R, N, fused):
     g = GpuPath(case, fused=fused)
     g.step()
     compare(g.results(), oracle_path(case))
+
+
+@pytest.mark.parametrize("alignment", [4, 128])
+def test_several_clusters_with_aligned_offsets(alignment):
+    """Several clusters with the fused, per-expert aligned offset scan (padding rows
+    at -1 in m_indices): the whole path against the oracle."""
+    from epd_paths import GpuPath, compare, oracle_path
+    case = workloads.make_random_case(T=12000, H=16, k=8, E=256, R=32, N=4, dtype="bf16",
+                                      seed=alignment + 7, routing="repeats", p_invalid=0.05,
+                                      experts="random")
+    g = GpuPath(case, fused=True, alignment=alignment)
+    g.step()
+    compare(g.results(), oracle_path(case, alignment=alignment))
+
+
+def test_several_clusters_without_optional_outputs():
+    """Several clusters with no tokens_per_rdma_rank and no is_token_in_rank: the
+    counts that are asked for, and the ranks, still match the oracle."""
+    dev = torch.device("cuda")
+    T, k = 16384, 8
+    case = _case(T, k, seed=71, routing="repeats")
+    ws = epd.new_workspace(T, k, E, R, N, dev)
+    st = epd.new_status(dev)
+    per_r, per_n, per_e, itr = epd.ep_dispatch_layout(case.topk_idx.to(dev), E, R, N, ws, st,
+                                                      with_rdma=False,
+                                                      with_is_token_in_rank=False)
+    assert per_n is None and itr is None
+    start, _ = epd.ep_scan_offsets(per_e, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want = oracle.dispatch_layout(case.topk_idx.numpy(), E, R, N)
+    assert np.array_equal(per_e.cpu().numpy(), want["tokens_per_expert"])
+    assert np.array_equal(per_r.cpu().numpy(), want["tokens_per_rank"])
+    _check_ranks(case, ws, st, start, "no optional outputs")
