@@ -364,6 +364,39 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint3
         : "memory");
 }
 
+// L2 eviction-priority policies for the cache hints below (fraction 1: every access
+// made with the policy).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Asks L2 to fetch `bytes` at `src` (16-byte aligned, a multiple of 16 bytes) with
+// the given eviction policy. A hint only: it changes no value any load returns (L2
+// is where every write lands), so it may be issued before the dependency wait.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+                 "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
+// bulk_load with an L2 eviction policy for the lines it reads.
+__device__ __forceinline__ void bulk_load_policy(void *dst_smem, const void *src, uint32_t bytes,
+                                                 uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // Shared -> global bulk copy in the current bulk group.
 __device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),

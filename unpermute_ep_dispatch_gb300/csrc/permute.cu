@@ -48,6 +48,9 @@ struct PermuteArgs {
     // column-major scales: the permute leaves each filled row's source token in
     // m_indices and scale_gather_kernel writes the scales and the final m_indices
     int defer_scales;
+    // whole expert range, bulk-copy kernel: blocks [0, pf_stride) (the first resident
+    // wave) prefetch the rows of blocks b, b + pf_stride, ... below pf_blocks into L2
+    int pf_stride, pf_blocks;
 };
 
 // m_indices over the whole buffer from the expert segments: row s belongs to the
@@ -225,6 +228,22 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         mbar_init_fence();
     }
+    // Before the dependency wait, the first resident wave asks L2 for the rows of the
+    // first blocks (up to kPrefetchBytes), marked to stay (evict-last): the layout kernel
+    // that usually runs just before is latency-bound and leaves HBM idle, and the
+    // prefetched lines outlast the rows this kernel writes meanwhile. A prefetch
+    // changes no value a load returns, so it is safe whatever ran before. Every row
+    // is then loaded with an evict-first policy, which releases the line.
+    if (whole && warp == 0 && (int)blockIdx.x < a.pf_stride) {
+        const uint64_t keep = l2_policy_evict_last();
+        for (int b = blockIdx.x; b < a.pf_blocks; b += a.pf_stride) {
+            const int tb = (int)((int64_t)a.T * b / gridDim.x);
+            const int te = (int)((int64_t)a.T * (b + 1) / gridDim.x);
+            for (int t = tb + lane; t < te; t += 32)
+                bulk_prefetch_l2(a.x + (int64_t)t * a.row_bytes, bytes, keep);
+        }
+    }
+    const uint64_t release = l2_policy_evict_first();
     pdl_wait();  // offsets and pair ranks come from the previous kernels
     // rows of the first batch loaded ahead (by thread 0)
     const int pre = whole ? min(S - 1, min(B, t_end - t_begin)) : 0;
@@ -232,8 +251,9 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
         if (whole) {
             for (int i = 0; i < pre; ++i) {
                 mbar_expect_tx(&bars[i], bytes);
-                bulk_load(stage + i * L.row_stride, a.x + (int64_t)(t_begin + i) * a.row_bytes,
-                          bytes, &bars[i]);
+                bulk_load_policy(stage + i * L.row_stride,
+                                 a.x + (int64_t)(t_begin + i) * a.row_bytes, bytes, &bars[i],
+                                 release);
             }
         }
         const bool ok = a.hdr->num_tokens == a.T && a.hdr->num_topk == a.k;
@@ -297,8 +317,9 @@ __global__ void __launch_bounds__(kTmaThreads) permute_tma_kernel(PermuteArgs a)
             auto load = [&](int i) {
                 const uint32_t r = seq + i, st = r % S;
                 mbar_expect_tx(&bars[st], bytes);
-                bulk_load(stage + st * L.row_stride, a.x + (int64_t)(b0 + token(i)) * a.row_bytes,
-                          bytes, &bars[st]);
+                bulk_load_policy(stage + st * L.row_stride,
+                                 a.x + (int64_t)(b0 + token(i)) * a.row_bytes, bytes, &bars[st],
+                                 release);
             };
             const int first = min(n, S - 1);
             if (lane == 0)
@@ -425,6 +446,13 @@ namespace {
 
 epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs);
 
+// Rows the bulk-copy kernel prefetches into L2 before its dependency wait (measured on
+// GB300, steps of layout -> permute -> combine: 32 MB gains 3.1 us at dsv3_fp8 and
+// 5.2 us at skew_bf16, as much as 48 or 64 MB, and costs least when nothing runs
+// before the permute to hide it; without the evict-last mark the prefetched lines
+// were gone by the time they were read).
+constexpr int64_t kPrefetchBytes = 32ll << 20;
+
 epd_status_t permute_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t cs) {
     // The separate pass pays off when the scattered stores it replaces are many:
     // more than 16 words per row (fp32 per-128 scales of a 4096-wide row and up;
@@ -499,6 +527,11 @@ epd_status_t permute_rows_launch(PermuteArgs &a, int64_t T, int k, cudaStream_t 
             }
             if (g > T) g = T;
             const int grid = (int)(g < 1 ? 1 : g);
+            // the L2 prefetch: the first wave's blocks, for up to kPrefetchBytes of rows
+            a.pf_stride = (int)slots;
+            const int64_t block_bytes = (T + grid - 1) / grid * a.row_bytes;
+            const int64_t pf = kPrefetchBytes / (block_bytes > 0 ? block_bytes : 1);
+            a.pf_blocks = (int)(pf < grid ? pf : grid);
             return launch_pdl(permute_tma_kernel, grid, kTmaThreads, L.total, cs, a);
         }
     }
@@ -543,6 +576,8 @@ epd_status_t permute_common(PermuteArgs &a, const void *x, int64_t row_bytes,
     a.m_indices = m_indices;
     a.output_index = output_index;
     a.status = status;
+    a.pf_stride = 0;  // no prefetch unless the bulk-copy launch sets it
+    a.pf_blocks = 0;
     return EPD_OK;
 }
 
