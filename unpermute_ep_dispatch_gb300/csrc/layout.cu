@@ -8,12 +8,15 @@
 //
 // The batch is cut into token tiles, one per block: the blocks of one
 // thread-block cluster for batches up to 16 x 8192 pairs (they exchange their
-// counts through distributed shared memory), else one block per tile of
-// layout_tile_pairs(E) pairs in ticket order (a block only ever waits on blocks
-// already running). Inside a tile:
-//   * each warp walks a contiguous run of the tile's (token, pick) pairs in
-//     row-major order, 32 at a time; lanes holding the same expert find each other
-//     through a per-warp shared-memory word per expert (each sets its lane bit,
+// counts through distributed shared memory) -- or of several clusters, where one
+// cluster of 16 would need eight 32-pair chunks per warp (each cluster's last block
+// publishes the cluster's counts in global memory for the later clusters) -- else
+// one block per tile of layout_tile_pairs(E) pairs in ticket order (a block only
+// ever waits on blocks already running). Inside a tile:
+//   * each warp zeroes its private histogram row while its picks are in flight,
+//     then walks a contiguous run of the tile's (token, pick) pairs in row-major
+//     order, 32 at a time; lanes holding the same expert find each other through a
+//     per-warp shared-memory word per expert (each clears it, sets its lane bit,
 //     then reads the word), and the lowest of them adds the group's size to the
 //     warp's private histogram; the picks are parked in shared memory for the
 //     token masks;
@@ -21,15 +24,17 @@
 //     gives each pair its rank among the tile's pairs of the same expert, in
 //     (t, j) order; beside it, other warps build each token's rank and node bit
 //     masks and count the tile's tokens per rank and per node;
-//   * the tile's counts (experts, ranks, nodes) reach the later tiles: in the
-//     cluster, by stores into their shared memory and one cluster barrier; else
-//     they are published and read with a single-pass decoupled look-back (a warp
-//     polls the states of up to 32 earlier tiles at once and stops at the
-//     nearest one that has published its inclusive prefix);
+//   * the tile's counts (experts, ranks, nodes) reach the later tiles: in a
+//     cluster, by stores into their shared memory and one cluster barrier (then,
+//     with several clusters, through the published cluster counts); else they are
+//     published and read with a single-pass decoupled look-back (a warp polls the
+//     states of up to 32 earlier tiles at once and stops at the nearest one that
+//     has published its inclusive prefix);
 //   * prefix + warp base + rank inside the warp = the pair's rank inside its
 //     expert over the whole batch, stored in the workspace for ep_permute;
-//   * the last tile (the last ticket, or the cluster's last block) writes the
-//     totals (and, for ep_dispatch_layout_offsets, the expert offsets).
+//   * the last tile (the last ticket, or the grid's last block) writes the totals
+//     (and, for ep_dispatch_layout_offsets, the expert offsets) from eight warps
+//     while the others store the pair ranks.
 // A tile-form call with a single tile takes no ticket and publishes nothing.
 // Every value is an integer sum, so the outputs are the same whichever order the
 // blocks run in. Waits are bounded: a wait that runs out sets EPD_ERR_TIMEOUT and
