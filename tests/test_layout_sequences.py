@@ -293,6 +293,8 @@ FORM_EDGES = [
     (9000, 8, 256, 32, 4),      # several clusters, the last tiles of the last one empty
     (16384, 8, 256, 32, 4),     # several clusters at the cluster form's largest batch
     (4000, 16, 1024, 32, 4),    # several clusters of 16-warp blocks (E > 512)
+    (1100, 64, 256, 32, 4),     # several clusters at k = 64 (tiles of 9 tokens)
+    (9000, 8, 90, 9, 3),        # several clusters, table look-ups for ranks and nodes
 ]
 
 
