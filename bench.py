@@ -547,6 +547,43 @@ def chained_launch_us(path, n=16, replays=4):
     return out
 
 
+def sets_record(name, dev, stream, sets=4, steps=20, peak=None):
+    """The headline step cycling `sets` distinct input and output sets (routing, rows,
+    expert outputs, permuted buffer, y): no input is reused within `sets` steps, so
+    nothing a step reads can still sit in L2 from the step that last used it."""
+    import torch
+    import unpermute_ep_dispatch_gb300 as epd
+    from unpermute_ep_dispatch_gb300 import workloads
+    paths = [DevicePath(workloads.make_case(name, seed=700 + i), dev, stream)
+             for i in range(sets)]
+    for p in paths:
+        p.step()
+    filler = torch.empty(1 << 28, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        filler.fill_(0.0)     # the device stays busy while the first steps are enqueued
+    a.record(stream)
+    for i in range(steps):
+        paths[i % sets].step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    for p in paths:
+        epd.check_status(p.status, f"{name} steps over {sets} input sets")
+    ms = a.elapsed_time(b) / steps
+    byt = paths[0].bytes()
+    pb = byt["ep_dispatch_layout_offsets"] + byt["ep_permute"] + byt["ep_unpermute"]
+    gbs = pb / (ms * 1e-3) / 1e9
+    rec = {"input_sets": sets, "steps": steps, "ms_per_step": round(ms, 5),
+           "tokens_per_s": paths[0].case.T / (ms * 1e-3), "path_bytes": pb,
+           "path_gbs": round(gbs, 1), "frac": round(gbs / peak, 4) if peak else None,
+           "note": f"distinct routing, rows, expert outputs and output buffers cycled every "
+                   f"step ({sets} sets)"}
+    del paths, filler
+    torch.cuda.empty_cache()
+    return rec
+
+
 def config_record(name, dev, stream, steps=20, peak=None):
     """A few timed steps of another workload (outside the headline's timed region):
     ms per step, tokens/s, path GB/s and fraction of the HBM peak."""
@@ -977,6 +1014,8 @@ def run_epd(args, rank, world, local):
         torch.cuda.empty_cache()
         clocks.set_phase("configs")
         configs = {}
+        configs["dsv3_fp8_4_sets"] = sets_record("dsv3_fp8", dev, stream, sets=4, steps=20,
+                                                 peak=peak)
         for other, st in (("prefill_bf16", 20), ("skew_bf16", 10), ("tiny", 50)):
             configs[other] = config_record(other, dev, stream, steps=st, peak=peak)
         lat, tot_ms, n_steps, pb, info = decode_latency(dev, pool=16, replays=128,
