@@ -49,6 +49,7 @@ struct SmallArgs {
     int scale_cols;
     const int64_t *topk;
     int T, k, E, R, N, epr, rpn, alignment;
+    int rank_shift, node_shift;  // log2(E/R), log2(R/N) when powers of two, else -1
     int32_t *per_expert, *per_rank, *per_node;
     uint8_t *in_rank;
     int32_t *start_out, *total_out;
@@ -278,17 +279,31 @@ __global__ void __launch_bounds__(kThreads) small_dispatch_kernel(SmallArgs a) {
         // by counting the columns of each warp's masks. Every block counts the whole
         // batch (a few hundred tokens); block 0 writes the counts.
         const bool words = (a.R & 3) == 0 && (reinterpret_cast<uintptr_t>(a.in_rank) & 3) == 0;
+        const bool fastm = a.rank_shift >= 0 && a.node_shift >= 0 && a.R <= 32 && a.N <= 32;
         for (int t0 = (warp - 4) * 32; t0 < a.T; t0 += 128) {
             const int t = t0 + lane;
             unsigned long long rm = 0, nm = 0;
             if (t < a.T) {
                 const int16_t *row = s_e + t * a.k;
-                for (int j = 0; j < a.k; ++j) {
-                    const int e = row[j];
-                    if (e < 0) continue;
-                    const int r = s_rank_of[e];
-                    rm |= 1ull << r;
-                    nm |= 1ull << s_node_of[r];
+                if (fastm) {  // shifts, 32-bit masks
+                    const int rs = a.rank_shift, ns = a.node_shift;
+                    uint32_t r32 = 0u, n32 = 0u;
+                    for (int j = 0; j < a.k; ++j) {
+                        const int e = row[j];
+                        const int r = e >> rs;
+                        r32 |= e >= 0 ? 1u << r : 0u;
+                        n32 |= e >= 0 ? 1u << (r >> ns) : 0u;
+                    }
+                    rm = r32;
+                    nm = n32;
+                } else {
+                    for (int j = 0; j < a.k; ++j) {
+                        const int e = row[j];
+                        if (e < 0) continue;
+                        const int r = s_rank_of[e];
+                        rm |= 1ull << r;
+                        nm |= 1ull << s_node_of[r];
+                    }
                 }
                 if (a.in_rank && t >= t_begin && t < t_end) {
                     uint8_t *dst = a.in_rank + (int64_t)t * a.R;
@@ -416,6 +431,13 @@ extern "C" epd_status_t ep_dispatch(const void *x, epd_dtype_t dtype, const floa
     a.R = R;
     a.N = N;
     a.epr = E / R;
+    auto log2_exact = [](int v) {
+        int b = 0;
+        while ((1 << b) < v) ++b;
+        return (1 << b) == v ? b : -1;
+    };
+    a.rank_shift = log2_exact(E / R);
+    a.node_shift = log2_exact(R / N);
     a.rpn = R / N;
     a.alignment = alignment;
     a.per_expert = tokens_per_expert;

@@ -292,14 +292,44 @@ __global__ void __launch_bounds__(W * 32, 1) layout_kernel(LayoutArgs a) {
     // (3) one lane per token, warps taken from the top so that they run beside the
     // scan above: the ranks and nodes the token reaches (read from its picks in
     // shared memory), as bit masks when R, N <= 64 (a token counts once per rank and
-    // once per node), and the tile's tokens per rank and per node by counting the
-    // columns of the warp's masks; for R or N above 64 each token counts its distinct
-    // ranks or nodes by comparing its picks
+    // once per node) -- 32-bit masks from shifts alone when R, N <= 32 and E/R, R/N
+    // are powers of two, the top-8 row as one 16-byte load -- and the tile's tokens
+    // per rank and per node by counting the columns of the warp's masks; for R or N
+    // above 64 each token counts its distinct ranks or nodes by comparing its picks
     const bool small_r = a.R <= 64, small_n = a.N <= 64;
+    const bool fastm = a.rank_shift >= 0 && a.node_shift >= 0 && a.R <= 32 && a.N <= 32;
     for (int base = (W - 1 - warp) * 32; base < ntok; base += kThreads) {
         const int tl = base + lane;
         unsigned long long rm = 0, nm = 0;
-        if (tl < ntok) {
+        if (tl < ntok && fastm) {
+            // shifts for rank and node, R, N <= 32: 32-bit masks, no table look-ups;
+            // top-8 rows loaded as one 16-byte vector
+            const int16_t *row = s_pick + tl * a.k;
+            uint32_t r32 = 0u, n32 = 0u;
+            const int rs = a.rank_shift, ns = a.node_shift;
+            if (a.k == 8) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(row);
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int e = (int)(int16_t)(wv[j >> 1] >> (16 * (j & 1)));
+                    const int r = e >> rs;
+                    r32 |= e >= 0 ? 1u << r : 0u;
+                    n32 |= e >= 0 ? 1u << (r >> ns) : 0u;
+                }
+            } else {
+                for (int j = 0; j < a.k; ++j) {
+                    const int e = row[j];
+                    const int r = e >> rs;
+                    r32 |= e >= 0 ? 1u << r : 0u;
+                    n32 |= e >= 0 ? 1u << (r >> ns) : 0u;
+                }
+            }
+            rm = r32;
+            nm = n32;
+            tok_rmask[tl] = rm;
+            tok_nmask[tl] = nm;
+        } else if (tl < ntok) {
             const int16_t *row = s_pick + tl * a.k;
             for (int j = 0; j < a.k; ++j) {
                 const int e = row[j];
