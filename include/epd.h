@@ -225,6 +225,10 @@ EPD_API epd_status_t ep_scan_offsets_aligned(const int32_t *tokens_per_expert, i
  *   capacity_rows <= INT32_MAX.
  * `workspace` must hold the layout of the same topk_idx (same T and k); a
  * mismatch sets EPD_ERR_INVALID_ARG in *status and writes nothing.
+ * Over the whole expert range the kernel asks L2 for up to 32 MB of x's first
+ * rows before it waits for the previous kernel on the stream (a prefetch: it
+ * changes no value any load returns), marked evict-last, and releases each line
+ * (evict-first) when it reads the row.
  */
 EPD_API epd_status_t ep_permute(const void *x, epd_dtype_t dtype, const float *x_scale,
                         const int64_t *topk_idx, int num_tokens, int num_topk, int hidden,
